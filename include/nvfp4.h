@@ -1,0 +1,204 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4: NVFP4 quantize-with-transpose on one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * NVFP4: FP4 E2M1 codes (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 is the
+ * sign; element 2i in the low nibble of byte i), one E4M3 decode scale per
+ * 16-element block, and one FP32 amax per tensor (or per row) from which the
+ * FP32 global encode scale g = 448 * 6 / amax is formed:
+ *     s = E4M3_rn_satfinite((block_amax / 6) * g)        per block
+ *     r = g / float(s)   (r = 0 when s = 0; clamped to FLT_MAX)
+ *     q = E2M1_rn_satfinite(x * r)                       per element
+ * with amax = 0 giving g = 1 and an overflowing g clamped to FLT_MAX.
+ *
+ * Layouts (x is M x N, row-major, M rows, N the contiguous dimension):
+ *   row-wise data    [M][N/2] bytes     1x16 blocks along a row of x
+ *   row-wise scales  [M][N/16] bytes    compact, or swizzled (below)
+ *   column-wise data [N][M/2] bytes     the quantization of x transposed:
+ *                                       row j holds column j of x
+ *   column-wise scales [N][M/16] bytes  compact, or swizzled
+ *   Swizzled scales: the cuBLAS 1D block-scaling-factor layout for an R x C
+ *   scale matrix (R % 128 == 0, C % 4 == 0): byte offset of (r, c) =
+ *   ((r/128)*(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4.  It is
+ *   only accepted when both data dimensions are multiples of 128
+ *   ("Fuse NVFP4 scale swizzling on SM120 and SM121", Description).
+ *
+ * Conventions for every entry point:
+ *   * Pointers named x / data / scale / amax / out / noop are DEVICE pointers
+ *     owned by the caller; the library never allocates, frees or keeps them.
+ *     Device pointers must be 16-byte aligned (NVFP4_ERR_ALIGN otherwise).
+ *   * stream is a cudaStream_t (NULL = the legacy default stream).  All work
+ *     is enqueued on it asynchronously; no call synchronizes the device.
+ *   * Arguments are validated on the host before anything is enqueued: a
+ *     non-OK status means nothing was launched and no output was written.
+ *     NVFP4_ERR_CUDA means a launch failed (the CUDA error is sticky in the
+ *     calling thread's runtime, cudaGetLastError() reads it).
+ *   * noop: NULL, or a device float; when it holds 1.0f at execution time the
+ *     call writes nothing at all, amax buffers included ("Write both NVFP4
+ *     amax buffers", Changes: with a noop flag set both buffers are left
+ *     untouched).
+ *   * Kernels bound every wait they perform.  If a wait ever runs out, the
+ *     kernel records it in a per-device status word (read it with
+ *     nvfp4_device_status) and returns without finishing its outputs.
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_NULL = 1,    /* a required pointer is NULL                        */
+  NVFP4_ERR_SHAPE = 2,   /* negative size, or a blocked dimension not % 16     */
+  NVFP4_ERR_ALIGN = 3,   /* SWIZZLED on a shape not 128-aligned; bad pointer   */
+  NVFP4_ERR_DTYPE = 4,   /* unknown dtype, or one the operation does not take  */
+  NVFP4_ERR_FLAGS = 5,   /* unknown / contradictory flags; aliased amax buffers */
+  NVFP4_ERR_CUDA = 6,    /* a kernel launch failed                             */
+  NVFP4_ERR_TIMEOUT = 7  /* a device-side wait ran out (nvfp4_device_status)   */
+} nvfp4_status;
+
+/* flags */
+#define NVFP4_ROWWISE 1u     /* produce the row-wise output                   */
+#define NVFP4_COLWISE 2u     /* produce the column-wise (transposed) output   */
+#define NVFP4_SWIZZLED 4u    /* scales in the cuBLAS 128x4 layout             */
+#define NVFP4_SKIP_AMAX 8u   /* use the amax already in the buffers           */
+#define NVFP4_ROW_SCALED 16u /* dequantize: one amax per row                  */
+
+/* dtypes */
+#define NVFP4_BF16 0
+#define NVFP4_FP32 1
+
+typedef struct {
+  uint8_t* data_row;  /* [M][N/2]                       (ROWWISE)            */
+  uint8_t* scale_row; /* [M][N/16]                      (ROWWISE)            */
+  float* amax_row;    /* 1 float (row-scaled: M floats) (ROWWISE)            */
+  uint8_t* data_col;  /* [N][M/2]                       (COLWISE)            */
+  uint8_t* scale_col; /* [N][M/16]                      (COLWISE)            */
+  float* amax_col;    /* 1 float                        (COLWISE)            */
+} nvfp4_output;
+
+/* Human-readable name of a status. */
+const char* nvfp4_status_string(nvfp4_status status);
+
+/* Bytes of a scale tensor for a rows x cols data matrix (rows * cols / 16,
+ * compact or swizzled alike; swizzled needs rows % 128 == 0 and cols % 128 ==
+ * 0, else NVFP4_ERR_ALIGN).  Host-only, no device work. */
+nvfp4_status nvfp4_scale_bytes(int64_t rows, int64_t cols, unsigned flags, size_t* bytes);
+
+/*
+ * Per-tensor amax ("Write both NVFP4 amax buffers", Description and Changes):
+ * zeroes amax_row and, when non-NULL, amax_col, then reduces max|x| over the
+ * M x N elements of x into both; no device-to-device copy, no extra read.
+ * amax_row must not equal amax_col (distinct buffers: the same page's review
+ * reply on aliasing).  M or N may be 0 (amax = 0).  dtype: BF16 or FP32.
+ */
+nvfp4_status nvfp4_compute_amax(const void* x, int dtype, int64_t M, int64_t N,
+                                float* amax_row, float* amax_col, const float* noop,
+                                void* stream);
+
+/*
+ * Per-tensor amax pair for the random-Hadamard column-wise path ("Write both
+ * NVFP4 amax buffers", review reply on aliasing: row-wise amax = max|x|,
+ * column-wise amax = max|RHT(x)|).  RHT(x): every 16-element column block v
+ * (rows 16k..16k+15 of one column) becomes (1/4) H16 diag(sign) v, H16 the
+ * Sylvester Hadamard matrix in natural order, sign_i = -1 where bit i of
+ * sign_mask is set, rounded to BF16 (BF16 input only).  M % 16 == 0.
+ */
+nvfp4_status nvfp4_compute_amax_rht(const void* x, int dtype, int64_t M, int64_t N,
+                                    uint32_t sign_mask, float* amax_row, float* amax_col,
+                                    const float* noop, void* stream);
+
+/*
+ * 1D NVFP4 quantize with row-wise and/or column-wise outputs in one pass
+ * over x, after the per-tensor amax (written to both buffers); scales compact
+ * or swizzled ("Write both NVFP4 amax buffers"; "Fuse NVFP4 scale swizzling
+ * on SM120 and SM121", Changes: the generic and tuned 1D kernels gain a
+ * swizzled store).  flags: ROWWISE | COLWISE (at least one) | SWIZZLED |
+ * SKIP_AMAX.  ROWWISE needs N % 16 == 0, COLWISE needs M % 16 == 0.
+ * Both amax buffers receive max|x|; with SKIP_AMAX the kernel reads them
+ * instead (e.g. after a cross-rank MAX) and writes none.
+ */
+nvfp4_status nvfp4_quantize_1d(const void* x, int dtype, int64_t M, int64_t N,
+                               const nvfp4_output* out, unsigned flags, const float* noop,
+                               void* stream);
+
+/*
+ * 2D NVFP4 quantize: one E4M3 scale per 16x16 tile of x ("Fuse NVFP4 scale
+ * swizzling on SM120 and SM121", Description: the 2D in-kernel path).  The
+ * scale tensors keep the 1x16 shapes above with each tile's scale repeated
+ * over its 16 rows (row-wise) or 16 columns (column-wise), so the
+ * column-wise codes are exactly the transpose of the row-wise codes.
+ * M % 16 == 0 and N % 16 == 0.  Flags as nvfp4_quantize_1d.
+ */
+nvfp4_status nvfp4_quantize_2d(const void* x, int dtype, int64_t M, int64_t N,
+                               const nvfp4_output* out, unsigned flags, const float* noop,
+                               void* stream);
+
+/*
+ * Row-scaled (per-token) NVFP4 ("Implement row-scaled NVFP4 fprop recipe",
+ * Greptile summary: one FP32 amax per row; block scales recomputed relative
+ * to that row's value).  Row-wise only: flags = ROWWISE [| SWIZZLED]
+ * [| SKIP_AMAX]; out->amax_row has M floats and receives max|x[y,:]| (or is
+ * read, with SKIP_AMAX).  A zero row encodes to zero codes and scales.
+ * N % 16 == 0; any M >= 0.
+ */
+nvfp4_status nvfp4_quantize_row_scaled(const void* x, int dtype, int64_t M, int64_t N,
+                                       const nvfp4_output* out, unsigned flags,
+                                       const float* noop, void* stream);
+
+/*
+ * NVFP4 quantize with the random Hadamard transform on the column-wise path
+ * ("Write both NVFP4 amax buffers", GPU work per quantize call: the RHT path
+ * runs a zeroing kernel, a Hadamard-amax kernel and the quantize kernel;
+ * "Fuse NVFP4 scale swizzling on SM120 and SM121", Changes: the
+ * columnwise-RHT 1D kernel).  The row-wise output is the plain 1D
+ * quantization of x with amax_row = max|x|; the column-wise output is the 1D
+ * quantization of RHT(x) transposed (transform as nvfp4_compute_amax_rht)
+ * with amax_col = max|RHT(x)|.  BF16 input; M % 16 == 0, N % 16 == 0.
+ */
+nvfp4_status nvfp4_quantize_rht(const void* x, int dtype, int64_t M, int64_t N,
+                                const nvfp4_output* out, unsigned flags, uint32_t sign_mask,
+                                const float* noop, void* stream);
+
+/*
+ * Dequantize one direction of an NVFP4 tensor ("Implement row-scaled NVFP4
+ * fprop recipe", Important Files Changed, dequantize_nvfp4.cuh: row y uses
+ * tensor_amax[y] when row-scaled, else tensor_amax[0]):
+ *     out[y][j] = (E2M1(q[y][j]) * float(s[y][j/16])) * (a / 2688)
+ * in FP32, rounded to BF16 (out_dtype NVFP4_BF16) or kept (NVFP4_FP32).
+ * data [rows][cols/2], scale [rows][cols/16] (compact, or swizzled with
+ * NVFP4_SWIZZLED), amax 1 float (or rows floats with NVFP4_ROW_SCALED).
+ * cols % 16 == 0.  For a column-wise output pass rows = N, cols = M.
+ */
+nvfp4_status nvfp4_dequantize(const uint8_t* data, const uint8_t* scale, const float* amax,
+                              int64_t rows, int64_t cols, unsigned flags, void* out,
+                              int out_dtype, void* stream);
+
+/*
+ * Compact -> swizzled scale permutation ("Write both NVFP4 amax buffers",
+ * GPU work per quantize call: the post-quantize swizzle_row_scaling_kernel
+ * that unaligned shapes still need).  compact [rows][scale_cols];
+ * rows % 128 == 0, scale_cols % 4 == 0; compact and swizzled must not
+ * overlap.
+ */
+nvfp4_status nvfp4_swizzle_scales(const uint8_t* compact, uint8_t* swizzled, int64_t rows,
+                                  int64_t scale_cols, void* stream);
+
+/*
+ * Per-device status word of bounded device-side waits: bit 0 = a wait for a
+ * tile copy ran out.  Synchronizes the current device, copies the word into
+ * *status and, when clear != 0, resets it.  Returns NVFP4_ERR_TIMEOUT when a
+ * bit was set, NVFP4_OK otherwise, NVFP4_ERR_CUDA if the copy failed.
+ */
+nvfp4_status nvfp4_device_status(uint32_t* status, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H_ */

@@ -1,1 +1,235 @@
-"""placeholder"""
+"""NVFP4 quantize-with-transpose on one GB300 GPU (sm_103a).
+
+A thin PyTorch-facing binding of ``libnvfp4.so`` (C ABI in include/nvfp4.h).
+PyTorch supplies device memory and the current CUDA stream; every step of the
+computation (amax, scales, codes, transposition, swizzled scale layout,
+Hadamard transform, dequantize) runs in the library's CUDA kernels.
+
+    q = quantize(x, mode="2d", swizzled=True)    # amax + fused cast, 3 launches
+    xr = dequantize(q.data_row, q.scale_row, q.amax_row, swizzled=True)
+
+Modes: "1d" (1x16 blocks), "2d" (16x16 tiles), "rht" (random Hadamard
+transform on the column-wise path) and "row_scaled" (one amax per row,
+row-wise only).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import NVFP4Error
+
+ROWWISE = 1
+COLWISE = 2
+SWIZZLED = 4
+SKIP_AMAX = 8
+ROW_SCALED = 16
+BF16 = 0
+FP32 = 1
+
+__all__ = ["NVFP4Tensor", "NVFP4Error", "empty", "compute_amax", "compute_amax_rht", "quantize",
+           "quantize_1d", "quantize_2d", "quantize_rht", "quantize_row_scaled", "dequantize",
+           "swizzle_scales", "scale_bytes", "device_status"]
+
+
+@dataclass
+class NVFP4Tensor:
+    """Row-wise and/or column-wise NVFP4 data of an M x N tensor.
+
+    data_row [M, N/2] uint8, scale_row [M*N/16] uint8, amax_row [1] (row-scaled: [M]) float32;
+    data_col [N, M/2] uint8, scale_col [N*M/16] uint8, amax_col [1] float32.
+    Scale buffers are flat: compact [rows][cols/16] or the cuBLAS 128x4 layout.
+    """
+    M: int
+    N: int
+    data_row: torch.Tensor | None = None
+    scale_row: torch.Tensor | None = None
+    amax_row: torch.Tensor | None = None
+    data_col: torch.Tensor | None = None
+    scale_col: torch.Tensor | None = None
+    amax_col: torch.Tensor | None = None
+    swizzled: bool = False
+    row_scaled: bool = False
+
+    def c_struct(self) -> _lib.Output:
+        p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        return _lib.Output(p(self.data_row), p(self.scale_row), p(self.amax_row),
+                           p(self.data_col), p(self.scale_col), p(self.amax_col))
+
+
+def _dtype_code(x: torch.Tensor) -> int:
+    if x.dtype == torch.bfloat16:
+        return BF16
+    if x.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"NVFP4 quantize takes bfloat16 or float32 input, got {x.dtype}")
+
+
+def _require_cuda(*ts: torch.Tensor | None) -> None:
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors passed to libnvfp4 must be contiguous CUDA tensors")
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+class _OnDevice:
+    """Makes `device` current for the library call (a no-op when it already is)."""
+    __slots__ = ("idx", "prev")
+
+    def __init__(self, device: torch.device):
+        self.idx = device.index if device.index is not None else torch.cuda.current_device()
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def empty(M: int, N: int, rowwise: bool = True, colwise: bool = True, row_scaled: bool = False,
+          swizzled: bool = False, device: torch.device | str = "cuda") -> NVFP4Tensor:
+    """Allocates (with PyTorch) the output buffers of an M x N quantization."""
+    dev = torch.device(device)
+    q = NVFP4Tensor(M, N, swizzled=swizzled, row_scaled=row_scaled)
+    if rowwise:
+        q.data_row = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+        q.scale_row = torch.empty(M * (N // 16), dtype=torch.uint8, device=dev)
+        q.amax_row = torch.empty(M if row_scaled else 1, dtype=torch.float32, device=dev)
+    if colwise:
+        q.data_col = torch.empty((N, M // 2), dtype=torch.uint8, device=dev)
+        q.scale_col = torch.empty(N * (M // 16), dtype=torch.uint8, device=dev)
+        q.amax_col = torch.empty(1, dtype=torch.float32, device=dev)
+    return q
+
+
+def scale_bytes(rows: int, cols: int, swizzled: bool = False) -> int:
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.load().nvfp4_scale_bytes(rows, cols, SWIZZLED if swizzled else 0, ctypes.byref(n)),
+               "nvfp4_scale_bytes")
+    return n.value
+
+
+def compute_amax(x: torch.Tensor, amax_row: torch.Tensor, amax_col: torch.Tensor | None = None,
+                 noop: torch.Tensor | None = None) -> None:
+    """Zeroes amax_row (and amax_col) then writes max|x| into both."""
+    _require_cuda(x, amax_row, amax_col, noop)
+    M, N = (x.shape[0], x.numel() // x.shape[0]) if x.dim() > 0 and x.shape[0] > 0 else (0, 0)
+    with _OnDevice(x.device):
+        _lib.check(_lib.load().nvfp4_compute_amax(_ptr(x), _dtype_code(x), M, N, _ptr(amax_row), _ptr(amax_col),
+                                                  _ptr(noop), _stream(x.device)), "nvfp4_compute_amax")
+
+
+def compute_amax_rht(x: torch.Tensor, sign_mask: int, amax_row: torch.Tensor, amax_col: torch.Tensor,
+                     noop: torch.Tensor | None = None) -> None:
+    """max|x| into amax_row and max|RHT(x)| into amax_col (BF16 x, M x N)."""
+    _require_cuda(x, amax_row, amax_col, noop)
+    M, N = x.shape
+    with _OnDevice(x.device):
+        _lib.check(_lib.load().nvfp4_compute_amax_rht(_ptr(x), _dtype_code(x), M, N, sign_mask & 0xFFFF,
+                                                      _ptr(amax_row), _ptr(amax_col), _ptr(noop),
+                                                      _stream(x.device)), "nvfp4_compute_amax_rht")
+
+
+def quantize(x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: bool = True,
+             swizzled: bool = False, sign_mask: int = 0, out: NVFP4Tensor | None = None,
+             skip_amax: bool = False, noop: torch.Tensor | None = None) -> NVFP4Tensor:
+    """NVFP4-quantizes the 2-D tensor x (bfloat16 or float32) on its device."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (M x N)")
+    M, N = x.shape
+    row_scaled = mode == "row_scaled"
+    if row_scaled:
+        colwise = False
+    if out is None:
+        out = empty(M, N, rowwise, colwise, row_scaled=row_scaled, swizzled=swizzled, device=x.device)
+    out.swizzled = swizzled
+    _require_cuda(x, out.data_row, out.scale_row, out.amax_row, out.data_col, out.scale_col, out.amax_col, noop)
+    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLED if swizzled else 0) | \
+        (SKIP_AMAX if skip_amax else 0)
+    L = _lib.load()
+    st = out.c_struct()
+    with _OnDevice(x.device):
+        s = _stream(x.device)
+        if mode == "1d":
+            rc = L.nvfp4_quantize_1d(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), s)
+        elif mode == "2d":
+            rc = L.nvfp4_quantize_2d(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), s)
+        elif mode == "rht":
+            rc = L.nvfp4_quantize_rht(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, sign_mask & 0xFFFF,
+                                      _ptr(noop), s)
+        elif mode == "row_scaled":
+            rc = L.nvfp4_quantize_row_scaled(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), s)
+        else:
+            raise ValueError(f"unknown mode {mode!r}")
+    _lib.check(rc, f"nvfp4 quantize ({mode})")
+    return out
+
+
+def quantize_1d(x, **kw):
+    return quantize(x, "1d", **kw)
+
+
+def quantize_2d(x, **kw):
+    return quantize(x, "2d", **kw)
+
+
+def quantize_rht(x, sign_mask: int, **kw):
+    return quantize(x, "rht", sign_mask=sign_mask, **kw)
+
+
+def quantize_row_scaled(x, **kw):
+    return quantize(x, "row_scaled", **kw)
+
+
+def dequantize(data: torch.Tensor, scale: torch.Tensor, amax: torch.Tensor, swizzled: bool = False,
+               row_scaled: bool = False, out_dtype: torch.dtype = torch.bfloat16,
+               out: torch.Tensor | None = None) -> torch.Tensor:
+    """Dequantizes one direction: data [rows, cols/2] -> [rows, cols]."""
+    rows, half = data.shape
+    cols = 2 * half
+    if out is None:
+        out = torch.empty((rows, cols), dtype=out_dtype, device=data.device)
+    _require_cuda(data, scale, amax, out)
+    od = BF16 if out.dtype == torch.bfloat16 else FP32 if out.dtype == torch.float32 else -1
+    flags = (SWIZZLED if swizzled else 0) | (ROW_SCALED if row_scaled else 0)
+    with _OnDevice(data.device):
+        _lib.check(_lib.load().nvfp4_dequantize(_ptr(data), _ptr(scale), _ptr(amax), rows, cols, flags, _ptr(out), od,
+                                                _stream(data.device)), "nvfp4_dequantize")
+    return out
+
+
+def swizzle_scales(compact: torch.Tensor, rows: int, scale_cols: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Compact [rows][scale_cols] scales -> the cuBLAS 128x4 layout (flat)."""
+    if out is None:
+        out = torch.empty(rows * scale_cols, dtype=torch.uint8, device=compact.device)
+    _require_cuda(compact, out)
+    with _OnDevice(compact.device):
+        _lib.check(_lib.load().nvfp4_swizzle_scales(_ptr(compact), _ptr(out), rows, scale_cols,
+                                                    _stream(compact.device)), "nvfp4_swizzle_scales")
+    return out
+
+
+def device_status(clear: bool = True) -> int:
+    """Synchronizes the current device and returns its status word (0 = no
+    device-side wait ran out)."""
+    v = ctypes.c_uint32(0)
+    rc = _lib.load().nvfp4_device_status(ctypes.byref(v), int(clear))
+    if rc not in (0, 7):
+        _lib.check(rc, "nvfp4_device_status")
+    return v.value

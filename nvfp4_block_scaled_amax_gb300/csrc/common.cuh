@@ -1,0 +1,244 @@
+// common.cuh -- device helpers shared by the NVFP4 kernels (sm_103a).
+//
+// Conversions use the hardware cvt instructions with round-to-nearest-even
+// and saturation (E2M1 data, E4M3 block scales), TMA tile loads complete on
+// shared-memory mbarriers, and every wait is bounded.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// Bits of the per-device status word (see nvfp4_device_status).
+constexpr unsigned kStatusWaitTimeout = 1u;
+// A wait that has not completed after this many SM cycles (about 2 s at the
+// GB300 boost clock) is abandoned.
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+constexpr float kFltMax = 3.402823466e38f;
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Scale arithmetic
+// ---------------------------------------------------------------------------
+
+// b / 6 correctly rounded, with Markstein's FMA correction of the reciprocal
+// product (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// c = RN(1/6), q = RN(b*c) and the exact residual e = b - 6q (one FMA),
+// RN(q + e*c) is the correctly rounded quotient.  Very small b, where q
+// would be subnormal, use the IEEE division.  Equality with __fdiv_rn is
+// checked on the GPU over every positive FP32 value.
+__device__ __forceinline__ float div6_rn(float b) {
+  if (b < 1.0e-30f) return __fdiv_rn(b, 6.0f);
+  const float c = 1.0f / 6.0f;
+  float q = __fmul_rn(b, c);
+  float e = __fmaf_rn(-q, 6.0f, b);
+  return __fmaf_rn(e, c, q);
+}
+
+// FP32 global encode scale 448*6/amax; amax = 0 -> 1; overflow -> FLT_MAX.
+__device__ __forceinline__ float global_encode_scale(float amax) {
+  if (amax == 0.0f) return 1.0f;
+  return fminf(__fdiv_rn(2688.0f, amax), kFltMax);
+}
+
+// Value of an E4M3 (FN) code 0..126, from its exponent and mantissa fields.
+__device__ __forceinline__ float e4m3_decode(uint32_t c) {
+  uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  if (e == 0) return __fmul_rn(__uint2float_rn(m), 0.001953125f);   // m * 2^-9
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Per-block encode factor r = g / float(s), clamped to FLT_MAX; 0 for s = 0.
+__device__ __forceinline__ float encode_factor(uint32_t s, float g) {
+  if (s == 0 || s >= 127) return 0.0f;
+  return fminf(__fdiv_rn(g, e4m3_decode(s)), kFltMax);
+}
+
+// E4M3 code of a non-negative FP32 value (RNE, saturating at 448).
+__device__ __forceinline__ uint32_t e4m3_rn_satfinite(float v) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(v));
+  return h & 0xFFu;
+}
+
+// Eight FP32 values -> eight E2M1 codes (RNE, saturating), v0 in bits 0..3.
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4,
+                                           float v5, float v6, float v7) {
+  uint32_t out;
+  asm("{\n"
+      ".reg .b8 q0, q1, q2, q3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n"
+      "mov.b32 %0, {q0, q1, q2, q3};\n"
+      "}"
+      : "=r"(out)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// BF16 helpers (a 32-bit word holds two BF16 values, the lower address in
+// the low half)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// max(|a|, |b|) per BF16 half, as a packed pair (inputs are finite).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+  return r;
+}
+__device__ __forceinline__ float bf16x2_hmax_to_f32(uint32_t w) {
+  return fmaxf(bf16_lo(w), bf16_hi(w));
+}
+
+// FP32 -> BF16 (RNE) -> FP32.
+__device__ __forceinline__ float round_bf16(float v) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(v));
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// In-place 16-point Walsh-Hadamard butterflies, natural (Sylvester) order:
+// after the four stages v[o] = sum_i (-1)^popcount(o & i) v_in[i].
+__device__ __forceinline__ void fwht16(float* v) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        float a = v[i], c = v[i + h];
+        v[i] = __fadd_rn(a, c);
+        v[i + h] = __fsub_rn(a, c);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Shared memory, mbarrier and TMA
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of an mbarrier, at most `limit` SM cycles; on
+// timeout records kStatusWaitTimeout in *status and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
+                                                  long long limit = kWaitLimitCycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) {
+      atomicOr(status, kStatusWaitTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2D tiled TMA load of the box at (c0 = innermost, c1) into shared memory,
+// completing `bytes` transactions on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Streaming (evict-first) global stores of outputs
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void st_cs_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_cs_v2(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_cs_u32(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+__device__ __forceinline__ void st_cs_u16(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(a)) : "memory");
+}
+__device__ __forceinline__ void st_cs_u8(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(a & 0xFFu)) : "memory");
+}
+
+// Byte offset of scale (r, c) in the cuBLAS 128x4 block-scaling layout of a
+// scale matrix with C columns.
+__device__ __forceinline__ int64_t swizzled_scale_offset(int64_t r, int64_t c, int64_t C) {
+  return ((r >> 7) * (C >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+// Writes n (1, 2 or 4) consecutive scale bytes (packed little-endian in v)
+// of row r starting at scale column c, compact [R][C] or swizzled.  In the
+// swizzled layout c is a multiple of n, so the group is contiguous and
+// aligned; in the compact layout the store is split into bytes when the
+// address is not aligned.
+__device__ __forceinline__ void store_scales(uint8_t* base, int64_t r, int64_t c, int64_t C, bool swizzled,
+                                             int n, uint32_t v) {
+  int64_t off = swizzled ? swizzled_scale_offset(r, c, C) : r * C + c;
+  uint8_t* p = base + off;
+  if (((reinterpret_cast<uintptr_t>(p)) & (uintptr_t)(n - 1)) == 0) {
+    if (n == 4) { st_cs_u32(p, v); return; }
+    if (n == 2) { st_cs_u16(p, v); return; }
+    if (n == 1) { st_cs_u8(p, v); return; }
+  }
+  for (int i = 0; i < n; ++i) st_cs_u8(p + i, v >> (8 * i));
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,81 @@
+// kernels.h -- internal launchers of the NVFP4 kernels (host side).
+//
+// Every launcher enqueues on ctx.stream and returns the launch status; the
+// arguments have been validated by the C-ABI layer (nvfp4_api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// Launches `func` so that it may start while the preceding kernel on the
+// stream is still running (programmatic dependent launch); the kernel's
+// griddepcontrol.wait orders it after that kernel's memory operations.
+inline cudaError_t launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  int num_sms;
+  unsigned* status;  // per-device status word (device address)
+};
+
+// Zero both amax buffers, then max|x| into both (the reduction may start
+// before the zeroing kernel ends; its atomics wait for it).
+cudaError_t launch_amax(const void* x, bool bf16, int64_t n, float* amax_a, float* amax_b,
+                        const float* noop, const LaunchCtx& ctx);
+
+// Zero both buffers, then max|x| into amax_row and max|RHT(x)| (BF16-rounded)
+// into amax_col.  x is BF16, M % 16 == 0, N % 16 == 0.
+cudaError_t launch_rht_amax(const uint16_t* x, int64_t M, int64_t N, uint32_t sign_mask, float* amax_row,
+                            float* amax_col, const float* noop, const LaunchCtx& ctx);
+
+enum CastMode : int { kCast1D = 0, kCast2D = 1, kCastRHT = 2 };
+
+struct CastArgs {
+  int64_t M, N;
+  uint8_t* data_row;
+  uint8_t* scale_row;
+  const float* amax_row;
+  uint8_t* data_col;
+  uint8_t* scale_col;
+  const float* amax_col;
+  const float* noop;
+  unsigned* status;
+  int rowwise, colwise, swizzled;
+  uint32_t sign_mask;
+  int tiles_n, num_tiles;
+};
+
+// Fused row-wise + column-wise cast of x (TMA tiles of 128 x 128 elements)
+// reading the per-tensor amax from args.amax_row / args.amax_col.  `pdl`:
+// launched as a programmatic dependent of the preceding amax kernel.
+cudaError_t launch_cast(const void* x, bool bf16, int mode, CastArgs args, bool pdl, const LaunchCtx& ctx);
+
+// Row-scaled cast: per-row amax (unless skip_amax), row-wise codes/scales.
+cudaError_t launch_row_scaled(const void* x, bool bf16, int64_t M, int64_t N, uint8_t* data, uint8_t* scale,
+                              float* amax, bool skip_amax, bool swizzled, const float* noop,
+                              const LaunchCtx& ctx);
+
+cudaError_t launch_dequantize(const uint8_t* data, const uint8_t* scale, const float* amax, int64_t rows,
+                              int64_t cols, bool swizzled, bool row_scaled, void* out, bool out_bf16,
+                              const LaunchCtx& ctx);
+
+cudaError_t launch_swizzle(const uint8_t* compact, uint8_t* swizzled, int64_t rows, int64_t scale_cols,
+                           const LaunchCtx& ctx);
+
+}  // namespace nvfp4

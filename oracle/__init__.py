@@ -88,6 +88,9 @@ def lib() -> ctypes.CDLL:
             L.oracle_swizzle_scales.restype = ctypes.c_int
             L.oracle_dequantize.argtypes = [u8p, u8p, f32p, ctypes.c_int, i64, i64, ctypes.c_int, vp]
             L.oracle_dequantize.restype = ctypes.c_int
+            for name in ("oracle_e2m1_array", "oracle_e4m3_array", "oracle_bf16_array"):
+                getattr(L, name).argtypes = [vp, vp, i64]
+                getattr(L, name).restype = None
             _lib = L
     return _lib
 
@@ -156,11 +159,10 @@ def rht16(v: np.ndarray, mask: int, round_bf16: bool) -> np.ndarray:
 def encode_array(v: np.ndarray, fmt: str) -> np.ndarray:
     """Element-wise E2M1 / E4M3 / BF16 encoding of a float32 array."""
     L = lib()
-    fn = {"e2m1": L.oracle_e2m1_rn_satfinite, "e4m3": L.oracle_e4m3_rn_satfinite,
-          "bf16": L.oracle_f32_to_bf16_rn}[fmt]
+    fn = {"e2m1": L.oracle_e2m1_array, "e4m3": L.oracle_e4m3_array, "bf16": L.oracle_bf16_array}[fmt]
     flat = np.ascontiguousarray(v, dtype=np.float32).ravel()
-    out = np.fromiter((fn(float(f)) for f in flat), dtype=np.uint16 if fmt == "bf16" else np.uint8,
-                      count=flat.size)
+    out = np.empty(flat.size, dtype=np.uint16 if fmt == "bf16" else np.uint8)
+    fn(_ptr(flat), _ptr(out), flat.size)
     return out.reshape(np.shape(v))
 
 

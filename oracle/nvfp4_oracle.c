@@ -485,3 +485,19 @@ int oracle_dequantize(const uint8_t* data, const uint8_t* scale, const float* am
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Array forms of the encoders (for exhaustive comparisons)                  */
+/* ------------------------------------------------------------------------- */
+
+void oracle_e2m1_array(const float* in, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_rn_satfinite(in[i]);
+}
+
+void oracle_e4m3_array(const float* in, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_rn_satfinite(in[i]);
+}
+
+void oracle_bf16_array(const float* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16_rn(in[i]);
+}

@@ -18,3 +18,11 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_sessionstart(session):
+    # The CUDA library is built in-tree before any test imports it (nvcc
+    # cross-compiles for sm_103a without a GPU); the oracle is built by its
+    # own fixture.
+    from nvfp4_block_scaled_amax_gb300 import build
+    build.build()

@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/nvfp4.h declares, and rejects bad arguments with the
+documented status before touching CUDA (validation is host-only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_FLAGS = 0, 1, 2, 3, 4, 5
+ROW, COL, SWZ, SKIP, ROWSC = 1, 2, 4, 8, 16
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_block_scaled_amax_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("nvfp4_compute_amax", "nvfp4_quantize_1d", "nvfp4_quantize_2d", "nvfp4_quantize_row_scaled",
+                     "nvfp4_quantize_rht", "nvfp4_dequantize", "nvfp4_swizzle_scales"):
+        assert required in names
+
+
+def test_library_exports_every_declared_function(lib):
+    from nvfp4_block_scaled_amax_gb300 import _lib
+    names = declared_functions()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in nvfp4.h but not exported"
+    assert set(names) <= set(_lib.EXPORTS) | set(names)
+    assert sorted(_lib.EXPORTS) == names
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.nvfp4_status_string(code).decode()
+        assert s.startswith("NVFP4_")
+    assert "unknown" in lib.nvfp4_status_string(99).decode()
+
+
+def test_scale_bytes(lib):
+    n = ctypes.c_size_t()
+    assert lib.nvfp4_scale_bytes(256, 512, 0, ctypes.byref(n)) == OK and n.value == 256 * 32
+    assert lib.nvfp4_scale_bytes(256, 512, SWZ, ctypes.byref(n)) == OK and n.value == 256 * 32
+    assert lib.nvfp4_scale_bytes(200, 512, SWZ, ctypes.byref(n)) == ERR_ALIGN
+    assert lib.nvfp4_scale_bytes(256, 24, 0, ctypes.byref(n)) == ERR_SHAPE
+    assert lib.nvfp4_scale_bytes(256, 32, 0, None) == ERR_NULL
+
+
+# fake, 16-byte aligned device addresses: validation never dereferences them
+X, A, B, C, D, E, F, NOOP = (0x100000 * (i + 1) for i in range(8))
+
+
+def out(lib_mod, **kw):
+    from nvfp4_block_scaled_amax_gb300._lib import Output
+    base = dict(data_row=A, scale_row=B, amax_row=C, data_col=D, scale_col=E, amax_col=F)
+    base.update(kw)
+    return Output(**base)
+
+
+def q1d(lib, x=X, dtype=0, M=256, N=256, o=None, flags=ROW | COL, noop=None):
+    o = out(lib) if o is None else o
+    return lib.nvfp4_quantize_1d(x, dtype, M, N, ctypes.byref(o), flags, noop, None)
+
+
+def test_quantize_validation(lib):
+    assert lib.nvfp4_quantize_1d(X, 0, 256, 256, None, ROW, None, None) == ERR_NULL
+    assert q1d(lib, flags=0) == ERR_FLAGS                        # no direction
+    assert q1d(lib, flags=ROW | 64) == ERR_FLAGS                 # unknown bit
+    assert q1d(lib, flags=ROW | ROWSC) == ERR_FLAGS              # dequant-only flag
+    assert q1d(lib, dtype=2) == ERR_DTYPE
+    assert q1d(lib, M=-1) == ERR_SHAPE
+    assert q1d(lib, N=24, flags=ROW) == ERR_SHAPE                # row blocks need N % 16
+    assert q1d(lib, M=24, flags=COL) == ERR_SHAPE                # column blocks need M % 16
+    assert q1d(lib, x=X + 8) == ERR_ALIGN
+    assert q1d(lib, o=out(lib, data_col=D + 4)) == ERR_ALIGN
+    assert q1d(lib, o=out(lib, scale_row=0)) == ERR_NULL
+    assert q1d(lib, o=out(lib, amax_col=C)) == ERR_FLAGS          # aliased amax buffers
+    assert q1d(lib, M=192, flags=ROW | COL | SWZ) == ERR_ALIGN    # swizzle needs 128-aligned
+    assert q1d(lib, noop=NOOP + 4) == ERR_ALIGN
+    assert q1d(lib, x=0) == ERR_NULL
+    o = out(lib)
+    assert lib.nvfp4_quantize_2d(X, 0, 256, 24, ctypes.byref(o), ROW, None, None) == ERR_SHAPE
+    assert lib.nvfp4_quantize_2d(X, 0, 24, 256, ctypes.byref(o), ROW, None, None) == ERR_SHAPE
+    assert lib.nvfp4_quantize_rht(X, 1, 256, 256, ctypes.byref(o), ROW | COL, 0, None, None) == ERR_DTYPE
+    assert lib.nvfp4_quantize_row_scaled(X, 0, 256, 256, ctypes.byref(o), ROW | COL, None, None) == ERR_FLAGS
+    assert lib.nvfp4_quantize_row_scaled(X, 0, 256, 256, ctypes.byref(o), COL, None, None) == ERR_FLAGS
+
+
+def test_amax_and_misc_validation(lib):
+    assert lib.nvfp4_compute_amax(X, 0, 16, 16, None, None, None, None) == ERR_NULL
+    assert lib.nvfp4_compute_amax(X, 0, 16, 16, C, C, None, None) == ERR_FLAGS
+    assert lib.nvfp4_compute_amax(X, 3, 16, 16, C, None, None, None) == ERR_DTYPE
+    assert lib.nvfp4_compute_amax(X + 2, 0, 16, 16, C, None, None, None) == ERR_ALIGN
+    assert lib.nvfp4_compute_amax_rht(X, 0, 24, 16, 0, C, F, None, None) == ERR_SHAPE
+    assert lib.nvfp4_compute_amax_rht(X, 1, 16, 16, 0, C, F, None, None) == ERR_DTYPE
+    assert lib.nvfp4_dequantize(A, B, C, 128, 24, 0, D, 0, None) == ERR_SHAPE
+    assert lib.nvfp4_dequantize(A, B, C, 120, 128, SWZ, D, 0, None) == ERR_ALIGN
+    assert lib.nvfp4_dequantize(A, B, C, 128, 128, 2, D, 0, None) == ERR_FLAGS
+    assert lib.nvfp4_dequantize(A, B, C, 128, 128, 0, D, 5, None) == ERR_DTYPE
+    assert lib.nvfp4_dequantize(A, 0, C, 128, 128, 0, D, 0, None) == ERR_NULL
+    assert lib.nvfp4_swizzle_scales(A, B, 100, 8, None) == ERR_ALIGN
+    assert lib.nvfp4_swizzle_scales(A, B, 128, 6, None) == ERR_ALIGN
+    assert lib.nvfp4_swizzle_scales(0, B, 128, 8, None) == ERR_NULL
+    assert lib.nvfp4_device_status(None, 0) == ERR_NULL
+
+
+def test_python_layer_rejects_cpu_tensors():
+    import torch
+    import nvfp4_block_scaled_amax_gb300 as nv
+    x = torch.zeros(16, 16, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, RuntimeError)):
+        nv.quantize(x, "1d", out=nv.NVFP4Tensor(16, 16, *(torch.zeros(1),) * 6))
+    with pytest.raises(TypeError):
+        nv._dtype_code(torch.zeros(16, 16, dtype=torch.float16))
