@@ -4,7 +4,7 @@
 Default workload: 2D NVFP4 quantize of an 8192 x 5120 BF16 N(0,1) matrix
 (seed 1), row-wise and column-wise outputs, scales in the cuBLAS 128x4
 layout.  One step = one full quantize call (amax + fused cast: every row of
-the hot path for this workload).  Bytes per step = input read once + FP4
+the hot path for this workload; for 1D/2D one persistent kernel launch).  Bytes per step = input read once + FP4
 codes + E4M3 scales written (3.125 B per element for BF16 row+col).
 
 Timing: W untimed warm-up steps; then K steps, each bracketed by CUDA events
@@ -229,19 +229,23 @@ def bench_ours(args, rank, world, local_rank):
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
-    gpu_launches = args.steps * (3 if spec["mode"] != "row_scaled" else 1)
+    single = spec["mode"] in ("1d", "2d")
+    gpu_launches = args.steps * (1 if single or spec["mode"] == "row_scaled" else 3)
 
-    # Per-kernel split of the same work (amax kernels, then the cast alone),
-    # also L2-flushed, for the dominant-kernel roofline.
+    # The same work through the two-pass path (zero + amax kernels, then the
+    # cast kernel), and its two halves, also L2-flushed: for comparison.
     split = {}
     if spec["mode"] != "row_scaled" and not args.no_split:
+        two = lambda: nv.quantize(x, spec["mode"], swizzled=spec["swizzled"], sign_mask=mask, out=q,  # noqa
+                                  path="two_pass")
         amax_fn = (lambda: nv.compute_amax_rht(x, mask, q.amax_row, q.amax_col)) if spec["mode"] == "rht" else \
             (lambda: nv.compute_amax(x, q.amax_row, q.amax_col))
         cast_fn = lambda: nv.quantize(x, spec["mode"], swizzled=spec["swizzled"], sign_mask=mask, out=q,  # noqa
                                       skip_amax=True)
-        ta = time_steps(amax_fn, args.steps, flush, stream)
+        split["two_pass_ms"] = statistics.mean(time_steps(two, args.steps, flush, stream))
+        split["amax_ms"] = statistics.mean(time_steps(amax_fn, args.steps, flush, stream))
         tc = []
-        for k in range(args.steps):   # the cast reads x after the amax pass, as in the fused call
+        for k in range(args.steps):   # the cast reads x after the amax pass, as in the two-pass call
             flush(k)
             amax_fn()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -250,8 +254,8 @@ def bench_ours(args, rank, world, local_rank):
             e.record(stream)
             tc.append((s, e))
         torch.cuda.synchronize()
-        tc = [s.elapsed_time(e) for s, e in tc]
-        split = {"amax_ms": statistics.mean(ta), "cast_ms": statistics.mean(tc)}
+        split["cast_ms"] = statistics.mean([s.elapsed_time(e) for s, e in tc])
+        split = {k: round(v, 5) for k, v in split.items()}
 
     # e2e: host buffers through the public API, copies inside the timed region
     e2e = None if args.no_e2e else bench_e2e(nv, spec, x_host, q, mask, args, dev, flush)
@@ -272,11 +276,13 @@ def bench_ours(args, rank, world, local_rank):
                    "bytes_per_step": bytes_step,
                    "l2": "flushed between steps (256 MiB write, then 256 MiB read of another buffer)",
                    "parallelism": f"replicas x{world} (one independent matrix per GPU)"},
-        "roofline": {"bound": "hbm", "kernel": "nvfp4_quantize (zero + amax + fused cast, one call)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "fused_kernel (one launch: amax, grid barrier, cast)" if single else
+                     "quantize call (zero + amax + cast kernels)",
                      "achieved": round(per_gpu, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(per_gpu / peak, 4), "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": ncu_traffic(args.workload), "split_ms": split},
+                     "traffic": ncu_traffic(args.workload), "two_pass_ms": split},
         "e2e": e2e,
         "gpu_launches": gpu_launches,
         "host_us_per_call": host_us,

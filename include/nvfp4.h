@@ -166,6 +166,31 @@ nvfp4_status nvfp4_quantize_rht(const void* x, int dtype, int64_t M, int64_t N,
                                 const float* noop, void* stream);
 
 /*
+ * Single-launch 1D / 2D quantize: the same results as nvfp4_quantize_1d /
+ * nvfp4_quantize_2d (amax written to both buffers, codes, scales), computed
+ * by one persistent kernel that reads x from HBM once: it reduces max|x|
+ * while staging tiles in shared memory, meets the other CTAs at a grid-wide
+ * barrier, then casts the staged tiles and re-reads the rest from L2.
+ * ("Write both NVFP4 amax buffers", Description: the reduction writes both
+ * buffers; "Fuse NVFP4 scale swizzling on SM120 and SM121": scales written
+ * directly in the GEMM layout.)
+ *   workspace: NVFP4_SINGLE_PASS_WORKSPACE_BYTES of device memory, zeroed
+ *   before its first use and not shared by calls that can run at the same
+ *   time; the kernel leaves it ready for the next call.  After a call that
+ *   reported NVFP4_ERR_TIMEOUT through nvfp4_device_status, zero it again.
+ *   flags: ROWWISE | COLWISE | SWIZZLED (no SKIP_AMAX: use the two-pass
+ *   entry points for a given amax).  All CTAs must be co-resident (one per
+ *   SM); a device where that is impossible returns NVFP4_ERR_CUDA.
+ */
+#define NVFP4_SINGLE_PASS_WORKSPACE_BYTES 256
+nvfp4_status nvfp4_quantize_1d_single_pass(const void* x, int dtype, int64_t M, int64_t N,
+                                           const nvfp4_output* out, unsigned flags, const float* noop,
+                                           void* workspace, void* stream);
+nvfp4_status nvfp4_quantize_2d_single_pass(const void* x, int dtype, int64_t M, int64_t N,
+                                           const nvfp4_output* out, unsigned flags, const float* noop,
+                                           void* workspace, void* stream);
+
+/*
  * Dequantize one direction of an NVFP4 tensor ("Implement row-scaled NVFP4
  * fprop recipe", Important Files Changed, dequantize_nvfp4.cuh: row y uses
  * tensor_amax[y] when row-scaled, else tensor_amax[0]):
@@ -191,7 +216,8 @@ nvfp4_status nvfp4_swizzle_scales(const uint8_t* compact, uint8_t* swizzled, int
 
 /*
  * Per-device status word of bounded device-side waits: bit 0 = a wait for a
- * tile copy ran out.  Synchronizes the current device, copies the word into
+ * tile copy ran out; bit 1 = a grid-wide barrier of a single-pass call ran
+ * out.  Synchronizes the current device, copies the word into
  * *status and, when clear != 0, resets it.  Returns NVFP4_ERR_TIMEOUT when a
  * bit was set, NVFP4_OK otherwise, NVFP4_ERR_CUDA if the copy failed.
  */

@@ -5,12 +5,18 @@ PyTorch supplies device memory and the current CUDA stream; every step of the
 computation (amax, scales, codes, transposition, swizzled scale layout,
 Hadamard transform, dequantize) runs in the library's CUDA kernels.
 
-    q = quantize(x, mode="2d", swizzled=True)    # amax + fused cast, 3 launches
+    q = quantize(x, mode="2d", swizzled=True)    # amax + fused cast, one launch
     xr = dequantize(q.data_row, q.scale_row, q.amax_row, swizzled=True)
 
 Modes: "1d" (1x16 blocks), "2d" (16x16 tiles), "rht" (random Hadamard
 transform on the column-wise path) and "row_scaled" (one amax per row,
 row-wise only).
+
+Paths for "1d" / "2d": "single_pass" (one persistent kernel: amax, grid
+barrier, cast; x read from HBM once; needs a small workspace, which this
+module keeps per device and stream) and "two_pass" (an amax kernel, then the
+cast kernel; needed for skip_amax).  "auto" picks single_pass when it
+applies.
 """
 from __future__ import annotations
 
@@ -31,6 +37,7 @@ BF16 = 0
 FP32 = 1
 
 __all__ = ["NVFP4Tensor", "NVFP4Error", "empty", "compute_amax", "compute_amax_rht", "quantize",
+           "single_pass_workspace", "reset_workspaces",
            "quantize_1d", "quantize_2d", "quantize_rht", "quantize_row_scaled", "dequantize",
            "swizzle_scales", "scale_bytes", "device_status"]
 
@@ -118,6 +125,27 @@ def empty(M: int, N: int, rowwise: bool = True, colwise: bool = True, row_scaled
     return q
 
 
+_workspaces: dict = {}
+
+
+def single_pass_workspace(device: torch.device, stream: int) -> torch.Tensor:
+    """The zero-initialised workspace of the single-pass kernels for one
+    device and stream (calls on one stream never overlap, so they may share
+    it; the kernels leave it ready for the next call)."""
+    key = (device.index, stream)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.zeros(_lib.SINGLE_PASS_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def reset_workspaces() -> None:
+    """Re-zeroes every cached workspace (after a reported device timeout)."""
+    for ws in _workspaces.values():
+        ws.zero_()
+
+
 def scale_bytes(rows: int, cols: int, swizzled: bool = False) -> int:
     n = ctypes.c_size_t(0)
     _lib.check(_lib.load().nvfp4_scale_bytes(rows, cols, SWIZZLED if swizzled else 0, ctypes.byref(n)),
@@ -148,8 +176,14 @@ def compute_amax_rht(x: torch.Tensor, sign_mask: int, amax_row: torch.Tensor, am
 
 def quantize(x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: bool = True,
              swizzled: bool = False, sign_mask: int = 0, out: NVFP4Tensor | None = None,
-             skip_amax: bool = False, noop: torch.Tensor | None = None) -> NVFP4Tensor:
-    """NVFP4-quantizes the 2-D tensor x (bfloat16 or float32) on its device."""
+             skip_amax: bool = False, noop: torch.Tensor | None = None, path: str = "auto",
+             workspace: torch.Tensor | None = None) -> NVFP4Tensor:
+    """NVFP4-quantizes the 2-D tensor x (bfloat16 or float32) on its device.
+
+    path: "auto" | "single_pass" | "two_pass" (1d / 2d only; see the module
+    docstring).  workspace: for the single-pass path, a zeroed uint8 CUDA
+    tensor of at least 256 bytes owned by the caller (default: one cached
+    per device and stream)."""
     if x.dim() != 2:
         raise ValueError("x must be 2-D (M x N)")
     M, N = x.shape
@@ -164,9 +198,19 @@ def quantize(x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: b
         (SKIP_AMAX if skip_amax else 0)
     L = _lib.load()
     st = out.c_struct()
+    if path not in ("auto", "single_pass", "two_pass"):
+        raise ValueError(f"unknown path {path!r}")
+    single = mode in ("1d", "2d") and not skip_amax and path != "two_pass"
+    if path == "single_pass" and not single:
+        raise ValueError("the single-pass path covers 1d / 2d quantize without skip_amax")
     with _OnDevice(x.device):
         s = _stream(x.device)
-        if mode == "1d":
+        if single:
+            ws = workspace if workspace is not None else single_pass_workspace(x.device, s.value)
+            _require_cuda(ws)
+            fn = L.nvfp4_quantize_1d_single_pass if mode == "1d" else L.nvfp4_quantize_2d_single_pass
+            rc = fn(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), _ptr(ws), s)
+        elif mode == "1d":
             rc = L.nvfp4_quantize_1d(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), s)
         elif mode == "2d":
             rc = L.nvfp4_quantize_2d(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), s)

@@ -51,11 +51,15 @@ __device__ __forceinline__ void publish_max(float m, float* a, float* b) {
 }
 
 // max|x| over n elements; x is 16-byte aligned.  nvec 16-byte vectors are
-// read by the grid-stride loop (four loads in flight per thread), the last
-// n - nvec*epv elements by block 0.
+// read by the grid-stride loop in batches of kUnroll independent loads per
+// thread (the last batch predicated, so no load waits behind another); one
+// resident wave of CTAs keeps ~128 KB of reads in flight per SM.  The last
+// n - nvec*epv elements are read by block 0.
+constexpr int kUnroll = 8;
+
 template <bool kBF16>
-__global__ void __launch_bounds__(kAmaxThreads) amax_reduce_kernel(const void* __restrict__ x, int64_t n,
-                                                                   float* a, float* b, const float* noop) {
+__global__ void __launch_bounds__(kAmaxThreads, 4) amax_reduce_kernel(const void* __restrict__ x, int64_t n,
+                                                                      float* a, float* b, const float* noop) {
   __shared__ float red[kAmaxThreads / 32];
   grid_launch_dependents();
   if (noop != nullptr && *noop == 1.0f) return;
@@ -74,12 +78,14 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_reduce_kernel(const void* _
       asm("max.bf16x2 %0, %0, %1;" : "+r"(acc0) : "r"(t0));
       asm("max.bf16x2 %0, %0, %1;" : "+r"(acc1) : "r"(t1));
     };
-    for (; i + 3 * stride < nvec; i += 4 * stride) {
-      uint4 v0 = ld_stream(xv + i), v1 = ld_stream(xv + i + stride);
-      uint4 v2 = ld_stream(xv + i + 2 * stride), v3 = ld_stream(xv + i + 3 * stride);
-      fold(v0); fold(v1); fold(v2); fold(v3);
+    for (; i < nvec; i += kUnroll * stride) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        v[u] = (i + u * stride < nvec) ? ld_stream(xv + i + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) fold(v[u]);
     }
-    for (; i < nvec; i += stride) fold(ld_stream(xv + i));
     uint32_t acc;
     asm("max.bf16x2 %0, %1, %2;" : "=r"(acc) : "r"(acc0), "r"(acc1));
     m = bf16x2_hmax_to_f32(acc);
@@ -94,12 +100,14 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_reduce_kernel(const void* _
       m0 = fmaxf(m0, fmaxf(fabsf(__uint_as_float(v.x)), fabsf(__uint_as_float(v.y))));
       m1 = fmaxf(m1, fmaxf(fabsf(__uint_as_float(v.z)), fabsf(__uint_as_float(v.w))));
     };
-    for (; i + 3 * stride < nvec; i += 4 * stride) {
-      uint4 v0 = ld_stream(xv + i), v1 = ld_stream(xv + i + stride);
-      uint4 v2 = ld_stream(xv + i + 2 * stride), v3 = ld_stream(xv + i + 3 * stride);
-      fold(v0); fold(v1); fold(v2); fold(v3);
+    for (; i < nvec; i += kUnroll * stride) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        v[u] = (i + u * stride < nvec) ? ld_stream(xv + i + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) fold(v[u]);
     }
-    for (; i < nvec; i += stride) fold(ld_stream(xv + i));
     m = fmaxf(m0, m1);
     if (blockIdx.x == 0) {
       const float* xs = static_cast<const float*>(x);
@@ -189,7 +197,7 @@ cudaError_t launch_amax(const void* x, bool bf16, int64_t n, float* amax_a, floa
     if (e != cudaSuccess) return e;
     occ[bf16].store(per_sm);
   }
-  int64_t want = (nvec + kAmaxThreads * 4 - 1) / (kAmaxThreads * 4);
+  int64_t want = (nvec + kAmaxThreads * kUnroll - 1) / (kAmaxThreads * kUnroll);
   int64_t cap = (int64_t)ctx.num_sms * (per_sm > 0 ? per_sm : 1);
   int grid = (int)(want < 1 ? 1 : (want > cap ? cap : want));
   void* args[] = {(void*)&x, (void*)&n, (void*)&amax_a, (void*)&amax_b, (void*)&noop};

@@ -1,87 +1,45 @@
 // cast.cu -- fused NVFP4 cast with row-wise and column-wise (transposed)
 // outputs from one read of each 128x128 tile of x.
 //
-// Per tile (TMA-loaded into shared memory with the 128-byte swizzle, a
-// multi-stage mbarrier pipeline, persistent CTAs walking the tiles in
-// reverse so the first ones hit the part of x the amax pass left in L2):
-//   row pass:    thread = one row x 64 columns (4 blocks of 1x16); block
-//                max, E4M3 scale, codes; 32 bytes of codes per thread.
-//   column pass: thread = 2 columns x 32 rows (BF16) or 1 column x 64 rows
-//                (FP32); the same per 16x1 block of x, i.e. per 1x16 block
-//                of x transposed.  With the random Hadamard transform the
-//                16 values of a column block are transformed first.
-//   2D:          one scale per 16x16 tile: the row pass reduces the block
-//                maxima over the tile's 16 rows (half-warp shuffles) and
-//                leaves the tile max in shared memory for the column pass.
-// Scales are stored compact or in the cuBLAS 128x4 layout ("Fuse NVFP4
-// scale swizzling on SM120 and SM121", Changes: groups of four scales as one
-// 32-bit store).  The encode factor g/float(s) comes from a 128-entry table
-// per CTA (one IEEE division per E4M3 code instead of one per block).
+// Tiles are TMA-loaded into shared memory (128-byte swizzle, a 3-stage
+// mbarrier pipeline); persistent CTAs walk the tiles in reverse order so the
+// first tiles they read are the ones the amax pass read last (most likely
+// still in L2).
+//
+// Per tile each thread owns an 8x8 sub-block (8 rows x 8 columns):
+//   * a 1x16 row block is the sub-blocks of lanes l and l^1; a 16x1 column
+//     block those of lanes l and l^8; a 16x16 tile lanes l, l^1, l^8, l^9;
+//     block maxima are combined with one or two shuffles;
+//   * row-wise codes: one 32-bit word (8 codes) per row of the sub-block;
+//   * column-wise codes: one word per column of the sub-block, computed from
+//     the same registers (1D, with the column block's scale) or, in 2D, the
+//     8x8 nibble transpose of the row-wise words (same scale per tile);
+//   * scales are staged in shared memory and stored once per tile by 128
+//     threads: 16-byte lines of the cuBLAS 128x4 layout ("Fuse NVFP4 scale
+//     swizzling on SM120 and SM121", Changes: aligned groups of four scales
+//     written together), or 8-byte runs of the compact layout.
+// With the random Hadamard transform the column-wise output comes from a
+// second pass over the tile in which each thread owns whole 16-row column
+// blocks (2 columns x 32 rows) and transforms them before the cast.
 #include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tile_ops.cuh"
 
 namespace nvfp4 {
 namespace {
 
+using namespace tile;
+
 constexpr int kThreads = 256;
-constexpr int kTile = 128;           // tile rows = tile columns (elements)
-constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 128 bytes
-
-template <typename T>
-struct TileCfg;
-template <>
-struct TileCfg<uint16_t> {
-  static constexpr int kEB = 2, kBoxCols = 64, kBoxes = 2, kStages = 3, kMinBlocks = 2;
-};
-template <>
-struct TileCfg<float> {
-  static constexpr int kEB = 4, kBoxCols = 32, kBoxes = 4, kStages = 3, kMinBlocks = 1;
-};
-
-template <typename T>
-__host__ __device__ constexpr int tile_bytes() {
-  return TileCfg<T>::kBoxes * kBoxBytes;
-}
-template <typename T>
-__host__ __device__ constexpr size_t smem_bytes() {
-  return 1024 + (size_t)TileCfg<T>::kStages * tile_bytes<T>() + 2 * 128 * 4 + 64 * 4 +
-         8 * TileCfg<T>::kStages + 16;
-}
-
-// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in box `box` of a
-// stage: the TMA 128-byte swizzle XORs the chunk index with row % 8.
-__device__ __forceinline__ uint32_t swz(int box, int row, int chunk) {
-  return (uint32_t)(box * kBoxBytes + row * 128 + (((chunk ^ row) & 7) << 4));
-}
-
-template <typename T>
-__device__ __forceinline__ float elem(const uint32_t* w, int i) {
-  if constexpr (sizeof(T) == 2)
-    return (i & 1) ? bf16_hi(w[i >> 1]) : bf16_lo(w[i >> 1]);
-  else
-    return __uint_as_float(w[i]);
-}
-
-// E4M3 scale code of a block with maximum b under global scale g.
-__device__ __forceinline__ uint32_t block_scale(float b, float g) {
-  return e4m3_rn_satfinite(__fmul_rn(div6_rn(b), g));
-}
-
-// 16 values times r -> two words of 8 E2M1 codes.
-__device__ __forceinline__ void encode16(const float* v, float r, uint32_t& lo, uint32_t& hi) {
-  lo = e2m1x8(__fmul_rn(v[0], r), __fmul_rn(v[1], r), __fmul_rn(v[2], r), __fmul_rn(v[3], r),
-              __fmul_rn(v[4], r), __fmul_rn(v[5], r), __fmul_rn(v[6], r), __fmul_rn(v[7], r));
-  hi = e2m1x8(__fmul_rn(v[8], r), __fmul_rn(v[9], r), __fmul_rn(v[10], r), __fmul_rn(v[11], r),
-              __fmul_rn(v[12], r), __fmul_rn(v[13], r), __fmul_rn(v[14], r), __fmul_rn(v[15], r));
-}
 
 struct Smem {
   uint8_t* stages;
   float* rtab_row;  // [128] encode factor per E4M3 code, row-wise g
   float* rtab_col;  // [128] same, column-wise g
-  float* tmax;      // [8][8] 16x16 tile maxima (2D)
+  uint8_t* sc_row;  // [2][128][8] staged row-wise scales of a tile (by tile parity)
+  uint8_t* sc_col;  // [2][128][8] staged column-wise scales
   uint64_t* bars;   // [kStages]
   int* abort_flag;
 };
@@ -94,168 +52,66 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   p += (size_t)TileCfg<T>::kStages * tile_bytes<T>();
   s.rtab_row = reinterpret_cast<float*>(p);
   s.rtab_col = s.rtab_row + 128;
-  s.tmax = s.rtab_col + 128;
-  s.bars = reinterpret_cast<uint64_t*>(s.tmax + 64);
+  s.sc_row = reinterpret_cast<uint8_t*>(s.rtab_col + 128);
+  s.sc_col = s.sc_row + 2048;
+  s.bars = reinterpret_cast<uint64_t*>(s.sc_col + 2048);
   s.abort_flag = reinterpret_cast<int*>(s.bars + TileCfg<T>::kStages);
   return s;
 }
 
 // ---------------------------------------------------------------------------
-// Row pass: thread (rr = tid % 128, h = tid / 128) owns tile row rr, tile
-// columns [64h, 64h + 64) = four 1x16 blocks.
+// Hadamard column pass (BF16): warp w -> box w % 2, rows 32 (w / 2) .. +32;
+// lane l -> tile columns 64 (w % 2) + 2l, +1; two 16-row blocks per column,
+// each transformed as (1/4) H16 diag(sign) v and rounded to BF16 before its
+// amax, scale and codes.
 // ---------------------------------------------------------------------------
-template <typename T, int MODE>
-__device__ __forceinline__ void row_pass(const uint8_t* st, const Smem& sm, const CastArgs& a, int64_t r0,
-                                         int64_t c0, float g_row) {
-  using C = TileCfg<T>;
-  const int tid = threadIdx.x;
-  const int rr = tid & 127, h = tid >> 7;
-  constexpr int kWords = 64 * C::kEB / 4;  // 32 (BF16) or 64 (FP32)
-  uint32_t w[kWords];
-#pragma unroll
-  for (int j = 0; j < kWords / 4; ++j) {
-    // BF16: box h, chunks 0..7.  FP32: boxes 2h, 2h+1, chunks 0..7 each.
-    const int box = (sizeof(T) == 2) ? h : 2 * h + (j >> 3);
-    const uint4 v = *reinterpret_cast<const uint4*>(st + swz(box, rr, j & 7));
-    w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
-  }
-  float b[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(elem<T>(w, 16 * k + i)));
-    b[k] = m;
-  }
-  if constexpr (MODE == kCast2D) {
-    // 16x16 tile max: the tile's 16 rows are the 16 lanes of this half-warp.
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) b[k] = fmaxf(b[k], __shfl_xor_sync(0xFFFFFFFFu, b[k], o));
-    if ((tid & 15) == 0) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sm.tmax[(rr >> 4) * 8 + 4 * h + k] = b[k];
-    }
-  }
-  const int64_t y = r0 + rr;
-  const int64_t cb = c0 + 64 * h;  // first column of this segment
-  if (!a.rowwise || y >= a.M || cb >= a.N) return;
-  uint32_t code[8];
-  uint32_t scales = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t s = block_scale(b[k], g_row);
-    const float r = sm.rtab_row[s];
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = elem<T>(w, 16 * k + i);
-    encode16(v, r, code[2 * k], code[2 * k + 1]);
-    scales |= s << (8 * k);
-  }
-  uint8_t* dst = a.data_row + y * (a.N / 2) + cb / 2;
-  const int nblk = (cb + 64 <= a.N) ? 4 : (int)((a.N - cb) / 16);
-  if (nblk == 4) {
-    if (((a.N / 2) & 15) == 0) {
-      st_cs_v4(dst, code[0], code[1], code[2], code[3]);
-      st_cs_v4(dst + 16, code[4], code[5], code[6], code[7]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) st_cs_v2(dst + 8 * k, code[2 * k], code[2 * k + 1]);
-    }
-    store_scales(a.scale_row, y, cb / 16, a.N / 16, a.swizzled, 4, scales);
-  } else {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (k < nblk) {
-        st_cs_v2(dst + 8 * k, code[2 * k], code[2 * k + 1]);
-        store_scales(a.scale_row, y, cb / 16 + k, a.N / 16, a.swizzled, 1, scales >> (8 * k));
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Column pass.  BF16: warp w -> box w % 2, rows 32 (w / 2) .. +32; lane l ->
-// tile columns 64 (w % 2) + 2l, +1; two 16-row blocks per column.
-// FP32: warp w -> box w % 4, rows 64 (w / 4) .. +64; lane l -> tile column
-// 32 (w % 4) + l; four 16-row blocks.
-// ---------------------------------------------------------------------------
-template <typename T, int MODE>
-__device__ __forceinline__ void col_pass(const uint8_t* st, const Smem& sm, const CastArgs& a, int64_t r0,
-                                         int64_t c0, float g_col, const float* sgn) {
-  using C = TileCfg<T>;
-  constexpr int kCols = (sizeof(T) == 2) ? 2 : 1;   // columns per thread
-  constexpr int kBlk = (sizeof(T) == 2) ? 2 : 4;    // 16-row blocks per column
-  constexpr int kRows = 16 * kBlk;
-  constexpr int kWarpsPerBox = 8 / C::kBoxes;
+__device__ __forceinline__ void rht_col_pass(const uint8_t* st, const Smem& sm, const CastArgs& a, int64_t r0,
+                                             int64_t c0, float g_col, const float* sgn, int parity) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int box = warp % C::kBoxes;
-  const int rbase = (warp / C::kBoxes) * kRows;  // first tile row
-  (void)kWarpsPerBox;
-  uint32_t w[kRows];
+  const int box = warp & 1;
+  const int rbase = (warp >> 1) * 32;
+  uint32_t w[32];
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    const int row = rbase + i;
-    w[i] = *reinterpret_cast<const uint32_t*>(st + swz(box, row, lane >> 2) + ((lane & 3) << 2));
+  for (int r = 0; r < 32; ++r) {
+    const int row = rbase + r;
+    w[r] = *reinterpret_cast<const uint32_t*>(st + swz(box, row, lane >> 2) + ((lane & 3) << 2));
   }
-  const int64_t rg = r0 + rbase;  // first row of x
+  const int64_t rg = r0 + rbase;
 #pragma unroll
-  for (int cc = 0; cc < kCols; ++cc) {
-    const int tcol = box * C::kBoxCols + kCols * lane + cc;  // tile column
+  for (int cc = 0; cc < 2; ++cc) {
+    const int tcol = box * 64 + 2 * lane + cc;
     const int64_t x = c0 + tcol;
-    uint32_t code[2 * kBlk];
-    uint32_t scales = 0;
+    uint32_t code[4];
 #pragma unroll
-    for (int blk = 0; blk < kBlk; ++blk) {
+    for (int blk = 0; blk < 2; ++blk) {
       float v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t word = w[16 * blk + i];
-        if constexpr (sizeof(T) == 2)
-          v[i] = cc ? bf16_hi(word) : bf16_lo(word);
-        else
-          v[i] = __uint_as_float(word);
+      for (int r = 0; r < 16; ++r) {
+        const uint32_t word = w[16 * blk + r];
+        v[r] = __fmul_rn(cc ? bf16_hi(word) : bf16_lo(word), sgn[r]);
       }
-      if constexpr (MODE == kCastRHT) {
+      fwht16(v);
+      float bm = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], sgn[i]);
-        fwht16(v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = round_bf16(v[i]);
-      }
-      float bm;
-      if constexpr (MODE == kCast2D) {
-        bm = sm.tmax[((rbase >> 4) + blk) * 8 + (tcol >> 4)];
-      } else {
-        bm = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(v[i]));
+      for (int r = 0; r < 16; ++r) {
+        v[r] = round_bf16(v[r]);
+        bm = fmaxf(bm, fabsf(v[r]));
       }
       const uint32_t s = block_scale(bm, g_col);
-      encode16(v, sm.rtab_col[s], code[2 * blk], code[2 * blk + 1]);
-      scales |= s << (8 * blk);
+      const float rf = sm.rtab_col[s];
+      code[2 * blk] = encode8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], rf);
+      code[2 * blk + 1] = encode8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15], rf);
+      sm.sc_col[parity * 1024 + tcol * 8 + (rbase >> 4) + blk] = (uint8_t)s;
     }
-    if (!a.colwise || x >= a.N || rg >= a.M) continue;
-    uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
-    const int nblk = (rg + kRows <= a.M) ? kBlk : (int)((a.M - rg) / 16);
-    if (nblk == kBlk) {
-      if (((a.M / 2) & 15) == 0) {
-#pragma unroll
-        for (int q = 0; q < kBlk / 2; ++q)
-          st_cs_v4(dst + 16 * q, code[4 * q], code[4 * q + 1], code[4 * q + 2], code[4 * q + 3]);
+    // M % 16 == 0: the first block is inside when rg < M, the second when
+    // rg + 16 < M.
+    if (x < a.N && rg < a.M) {
+      uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
+      if (rg + 32 <= a.M && ((a.M / 2) & 15) == 0) {
+        st_cs_v4(dst, code[0], code[1], code[2], code[3]);
       } else {
-#pragma unroll
-        for (int q = 0; q < kBlk; ++q) st_cs_v2(dst + 8 * q, code[2 * q], code[2 * q + 1]);
-      }
-      store_scales(a.scale_col, x, rg / 16, a.M / 16, a.swizzled, kBlk, scales);
-    } else {
-#pragma unroll
-      for (int q = 0; q < kBlk; ++q) {
-        if (q < nblk) {
-          st_cs_v2(dst + 8 * q, code[2 * q], code[2 * q + 1]);
-          store_scales(a.scale_col, x, rg / 16 + q, a.M / 16, a.swizzled, 1, scales >> (8 * q));
-        }
+        st_cs_v2(dst, code[0], code[1]);
+        if (rg + 16 < a.M) st_cs_v2(dst + 8, code[2], code[3]);
       }
     }
   }
@@ -310,10 +166,12 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
   for (int i = 0; i < 16; ++i) sgn[i] = ((a.sign_mask >> i) & 1u) ? -0.25f : 0.25f;
   __syncthreads();
 
+  const bool do_row = a.rowwise != 0;
+  const bool do_col_blk = a.colwise != 0 && MODE != kCastRHT;
   int k = 0;
   for (; k < my_count; ++k) {
     const int s = k % C::kStages;
-    // Warp-uniform so that the shuffles of the row pass see whole warps.
+    // Warp-uniform so that the shuffles below see whole warps.
     const bool ok =
         __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.bars[s], (uint32_t)((k / C::kStages) & 1), a.status));
     if (!ok) *sm.abort_flag = 1;
@@ -321,19 +179,31 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
     const int tr = t / a.tiles_n, tc = t - tr * a.tiles_n;
     const int64_t r0 = (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
     const uint8_t* st = sm.stages + (size_t)s * tile_bytes<T>();
-    if (ok && (a.rowwise || MODE == kCast2D)) row_pass<T, MODE>(st, sm, a, r0, c0, g_row);
-    if constexpr (MODE == kCast2D) __syncthreads();
-    if (ok && a.colwise) col_pass<T, MODE>(st, sm, a, r0, c0, g_col, sgn);
-    __syncthreads();  // stage s fully read
+    const int parity = k & 1;
+    if (ok && (do_row || do_col_blk))
+      block_pass_any<T, MODE>(smem_u32(st), sm.rtab_row, sm.rtab_col, smem_u32(sm.sc_row + parity * 1024),
+                              smem_u32(sm.sc_col + parity * 1024), a, r0, c0, g_row, g_col, do_row, do_col_blk,
+                              threadIdx.x >> 5);
+    if constexpr (MODE == kCastRHT) {
+      if (ok && a.colwise) rht_col_pass(st, sm, a, r0, c0, g_col, sgn, parity);
+    }
+    __syncthreads();  // stage s fully read; this tile's scales staged
     if (*sm.abort_flag) break;
     if (tid == 0 && k + C::kStages < my_count) issue(k + C::kStages);
+    // this tile's scales: threads 0..127 row-wise, 128..255 column-wise
+    if (tid < 128) {
+      if (do_row)
+        store_scale_tile(sm.sc_row + parity * 1024, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, tid);
+    } else if (a.colwise) {
+      store_scale_tile(sm.sc_col + parity * 1024, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, tid - 128);
+    }
   }
   if (k < my_count && tid == 0) {
     // A wait ran out: wait (bounded) for this CTA's copies still in flight
     // before the shared memory is released.
     const int issued = (k + C::kStages < my_count) ? k + C::kStages : my_count;
-    for (int j = k; j < issued; ++j)
-      mbar_wait_bounded(&sm.bars[j % C::kStages], (uint32_t)((j / C::kStages) & 1), a.status);
+    for (int jj = k; jj < issued; ++jj)
+      mbar_wait_bounded(&sm.bars[jj % C::kStages], (uint32_t)((jj / C::kStages) & 1), a.status);
   }
 }
 

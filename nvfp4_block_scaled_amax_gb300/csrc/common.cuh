@@ -12,7 +12,8 @@
 namespace nvfp4 {
 
 // Bits of the per-device status word (see nvfp4_device_status).
-constexpr unsigned kStatusWaitTimeout = 1u;
+constexpr unsigned kStatusWaitTimeout = 1u;  // a wait for a tile copy ran out
+constexpr unsigned kStatusGridTimeout = 2u;  // a grid-wide barrier ran out
 // A wait that has not completed after this many SM cycles (about 2 s at the
 // GB300 boost clock) is abandoned.
 constexpr long long kWaitLimitCycles = 4000000000LL;
@@ -151,10 +152,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// One bounded try: the thread may be suspended (up to ~0.1 ms) until the
+// phase completes, so a waiting warp costs few issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 100000;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
@@ -175,6 +178,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
   }
   return true;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -210,6 +219,16 @@ __device__ __forceinline__ void st_cs_v2(void* p, uint32_t a, uint32_t b) {
 }
 __device__ __forceinline__ void st_cs_u32(void* p, uint32_t a) {
   asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+// The same, executed only when `pred` is non-zero (a predicated store, no
+// branch).
+__device__ __forceinline__ void st_cs_u32_if(void* p, uint32_t a, uint32_t pred) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q st.global.cs.u32 [%0], %1;\n}" ::"l"(p), "r"(a),
+               "r"(pred)
+               : "memory");
+}
+__device__ __forceinline__ void sts_u8(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void st_cs_u16(void* p, uint32_t a) {
   asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(a)) : "memory");

@@ -1,0 +1,347 @@
+// fused.cu -- single-launch NVFP4 quantize: per-tensor amax and the fused
+// row-wise + column-wise cast in one persistent kernel.
+//
+// One CTA per SM (cooperative launch, all CTAs co-resident), 16 warps in two
+// groups of 8; a group casts one 128x128 tile at a time:
+//   * a stage's TMA completion is an mbarrier; when the 8 warps of a group
+//     are done with a stage, the last of them (a shared-memory counter per
+//     stage) writes the tile's staged scales back and issues the next load
+//     into the stage, so no warp ever waits for the whole CTA;
+//   * phase A streams the CTA's tiles t_k = blockIdx + k * gridDim through
+//     the stage ring computing max|x|; the last kStages tiles stay in shared
+//     memory;
+//   * a grid barrier in the caller's workspace combines the CTA maxima
+//     (the amax is written to both direction buffers, "Write both NVFP4 amax
+//     buffers");
+//   * phase B casts the resident tiles first, then reloads the others in
+//     reverse order (most recently read first, so mostly from L2; phase A
+//     marked them evict-last), writing codes, and scales in the compact or
+//     cuBLAS 128x4 layout.
+// x is read from HBM once; the call is one launch.
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tile_ops.cuh"
+
+namespace nvfp4 {
+namespace {
+
+using namespace tile;
+
+constexpr int kGroups = 2;                       // warp groups
+constexpr int kWarps = 8 * kGroups;              // 8 warps cast one tile
+constexpr int kFusedThreads = 32 * kWarps;
+
+template <typename T>
+struct FusedCfg;
+template <>
+struct FusedCfg<uint16_t> {
+  static constexpr int kStages = 6;  // even: stage parity = consumer group
+};
+template <>
+struct FusedCfg<float> {
+  static constexpr int kStages = 2;
+};
+
+template <typename T>
+__host__ __device__ constexpr size_t fused_smem_bytes() {
+  return 1024 + (size_t)FusedCfg<T>::kStages * (tile_bytes<T>() + 2048) + 2 * 128 * 4 +
+         16 * FusedCfg<T>::kStages + 64 * 4 + 64;
+}
+
+struct FSmem {
+  uint8_t* stages;   // [S][tile]
+  uint8_t* sc;       // [S][2][1024] staged row / column scales of the tile in stage s
+  float* rtab_row;   // [128]
+  float* rtab_col;   // [128]
+  uint64_t* full;    // [S]
+  unsigned* done;    // [S] warps of the current group done with the stage
+  unsigned* issued;  // [S] loads issued into the stage so far
+  float* red;        // [64]
+  float* amax;       // [1] broadcast of the global amax
+  int* abort_flag;   // [1]
+};
+
+template <typename T>
+__device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
+  constexpr int S = FusedCfg<T>::kStages;
+  FSmem s;
+  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023);
+  s.stages = p;
+  p += (size_t)S * tile_bytes<T>();
+  s.sc = p;
+  p += (size_t)S * 2048;
+  s.rtab_row = reinterpret_cast<float*>(p);
+  s.rtab_col = s.rtab_row + 128;
+  s.full = reinterpret_cast<uint64_t*>(s.rtab_col + 128);
+  s.done = reinterpret_cast<unsigned*>(s.full + S);
+  s.issued = s.done + S;
+  s.red = reinterpret_cast<float*>(s.issued + S);
+  s.amax = s.red + 64;
+  s.abort_flag = reinterpret_cast<int*>(s.amax + 1);
+  return s;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide maximum of one non-negative float per CTA (called by one thread
+// per CTA).  Generation-counted so the workspace needs no clearing between
+// calls: call g accumulates into acc[g & 1]; its last arriver resets the
+// arrival count and acc[(g + 1) & 1] for the next call, then publishes
+// g + 1.  The spin is bounded; false means it ran out.
+__device__ bool grid_max(SinglePassWorkspace* ws, float m, unsigned n_cta, unsigned* status, float* out) {
+  const unsigned gen = ld_acquire_gpu(&ws->gen);
+  atomicMax(&ws->acc[gen & 1u], __float_as_uint(m));
+  __threadfence();
+  const unsigned arrived = atomicAdd(&ws->count, 1u);
+  if (arrived == n_cta - 1) {
+    atomicExch(&ws->count, 0u);
+    atomicExch(&ws->acc[(gen + 1u) & 1u], 0u);
+    __threadfence();
+    atomicExch(&ws->gen, gen + 1u);
+  } else {
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(&ws->gen) == gen) {
+      if (clock64() - t0 > kWaitLimitCycles) {
+        atomicOr(status, kStatusGridTimeout);
+        return false;
+      }
+      __nanosleep(64);
+    }
+  }
+  __threadfence();
+  *out = __uint_as_float(atomicAdd(&ws->acc[gen & 1u], 0u));
+  return true;
+}
+
+// max|x| over this thread's 8x8 sub-block of a staged tile (as a packed pair
+// for BF16, a float for FP32).
+template <typename T>
+__device__ __forceinline__ float sub_absmax(uint32_t stage, int cw) {
+  const int lane = threadIdx.x & 31;
+  const int bx = cw & 1, q = cw >> 1, j = lane & 7, i = lane >> 3;
+  Sub<T> s;
+  load_sub<T>(stage, bx, 32 * q + 8 * i, j, s);
+  if constexpr (sizeof(T) == 2) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc = xsa(acc, xsa(xsa(s.w[k][0], s.w[k][1]), xsa(s.w[k][2], s.w[k][3])));
+    acc &= 0x7FFF7FFFu;
+    return fmaxf(bf16_lo(acc), bf16_hi(acc));
+  } else {
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) m = fmaxf(m, fabsf(s.v(k, c)));
+    return m;
+  }
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    fused_kernel(const __grid_constant__ CUtensorMap tmap, const CastArgs a, SinglePassWorkspace* ws) {
+  constexpr int S = FusedCfg<T>::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const FSmem sm = fcarve<T>(smem_raw);
+  if (a.noop != nullptr && *a.noop == 1.0f) return;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, b = blockIdx.x;
+  const int n = (a.num_tiles - 1 - b) / G + 1;  // tiles t_k = b + k * G, k < n (grid <= tiles)
+  const int kept_from = n > S ? n - S : 0;      // tiles k >= kept_from stay staged after phase A
+  auto tile_rc = [&](int k, int64_t& r0, int64_t& c0) {
+    const int t = b + k * G;
+    const int tr = t / a.tiles_n, tc = t - tr * a.tiles_n;
+    r0 = (int64_t)tr * kTile;
+    c0 = (int64_t)tc * kTile;
+  };
+
+  const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+  // Loads: phase A reads tiles 0..n-1 (the ones reloaded in phase B are kept
+  // in L2 with evict-last), phase B reloads tiles kept_from-1 .. 0.
+  auto issue = [&](int k, uint64_t pol) {
+    const int s = k % S;
+    int64_t r0, c0;
+    tile_rc(k, r0, c0);
+    uint8_t* dst = sm.stages + (size_t)s * tile_bytes<T>();
+    sm.issued[s] += 1;
+    mbar_arrive_expect_tx(&sm.full[s], tile_bytes<T>());
+#pragma unroll
+    for (int bb = 0; bb < TileCfg<T>::kBoxes; ++bb)
+      tma_load_2d(dst + bb * kBoxBytes, &tmap, (int32_t)c0 + bb * TileCfg<T>::kBoxCols, (int32_t)r0, &sm.full[s],
+                  pol);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sm.full[s], 1);
+      sm.done[s] = 0;
+      sm.issued[s] = 0;
+    }
+    *sm.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap);
+    for (int k = 0; k < S && k < n; ++k) issue(k, k >= kept_from ? stream : keep);
+  }
+  __syncthreads();
+
+  // A warp done with stage s counts itself; the 8th (last) warp of the group
+  // may then reuse the stage: it runs `refill` with all 32 lanes.  The fences
+  // make the other warps' shared-memory reads and staged scales happen
+  // before the refill.
+  auto finish_stage = [&](int s, auto&& refill) {
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = (atomicAdd(&sm.done[s], 1u) == 7u) ? 1u : 0u;
+      if (last) {
+        sm.done[s] = 0;
+        __threadfence_block();
+      }
+    }
+    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+      __syncwarp();  // the lanes' reads below come after lane 0's acquire
+      refill();
+    }
+  };
+
+  const int grp = warp >> 3, cw = warp & 7;
+  unsigned full_par = 0;  // bit s: parity of the next load of stage s (this group's stages)
+  bool ok = true;
+  auto wait_full = [&](int s) {
+    const bool w = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.full[s], (full_par >> s) & 1u, a.status));
+    full_par ^= 1u << s;
+    return w;
+  };
+
+  // phase A: max|x| of this group's tiles (k == grp mod 2; stage k % S has
+  // the same parity because S is even)
+  float m = 0.0f;
+  for (int k = grp; k < n; k += kGroups) {
+    const int s = k % S;
+    if (!wait_full(s)) {
+      ok = false;
+      break;
+    }
+    m = fmaxf(m, sub_absmax<T>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), cw));
+    if (k + S < n) {  // tile k leaves shared memory: load tile k + S into its stage
+      finish_stage(s, [&] {
+        if (lane == 0) issue(k + S, k + S >= kept_from ? stream : keep);
+      });
+    }
+  }
+  if (!ok) *sm.abort_flag = 1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) sm.red[warp] = m;
+  __syncthreads();
+  if (tid == 0) {
+    float cm = 0.0f;
+    for (int w = 0; w < kWarps; ++w) cm = fmaxf(cm, sm.red[w]);
+    float amax = 0.0f;
+    // A CTA that lost a wait still arrives, so the others are not held up.
+    const bool gok = grid_max(ws, cm, (unsigned)G, a.status, &amax);
+    if (!gok) *sm.abort_flag = 1;
+    *sm.amax = amax;
+    if (b == 0 && gok && !*sm.abort_flag) {
+      if (a.amax_row) *const_cast<float*>(a.amax_row) = amax;
+      if (a.amax_col) *const_cast<float*>(a.amax_col) = amax;
+    }
+    const float g = global_encode_scale(amax);
+    *sm.amax = g;
+  }
+  __syncthreads();
+  if (*sm.abort_flag) {
+    // let this CTA's copies in flight (the last load into each stage) land,
+    // bounded, before leaving
+    if (tid == 0)
+      for (int s = 0; s < S; ++s)
+        if (sm.issued[s] > 0) mbar_wait_bounded(&sm.full[s], (sm.issued[s] - 1u) & 1u, a.status);
+    return;
+  }
+  const float g = *sm.amax;
+  if (tid < 128)
+    sm.rtab_row[tid] = encode_factor((uint32_t)tid, g);
+  else if (tid < 256)
+    sm.rtab_col[tid - 128] = encode_factor((uint32_t)(tid - 128), g);
+  __syncthreads();
+
+  // phase B: descending k, this group's tiles; the last warp done with a
+  // tile writes its scales back and reloads tile k - S into the stage
+  const bool do_row = a.rowwise != 0, do_col = a.colwise != 0;
+  const int k_top = ((n - 1) & 1) == grp ? n - 1 : n - 2;
+  for (int k = k_top; k >= 0; k -= kGroups) {
+    const int s = k % S;
+    if (k < kept_from && !wait_full(s)) return;  // the waiting CTA gives up; outputs unfinished
+    int64_t r0, c0;
+    tile_rc(k, r0, c0);
+    uint8_t* sc = sm.sc + (size_t)s * 2048;
+    block_pass_any<T, MODE>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), sm.rtab_row, sm.rtab_col,
+                            smem_u32(sc), smem_u32(sc + 1024), a, r0, c0, g, g, do_row, do_col, cw);
+    finish_stage(s, [&] {
+      for (int t = lane; t < 128; t += 32) {
+        if (do_row) store_scale_tile(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
+        if (do_col) store_scale_tile(sc + 1024, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
+      }
+      __syncwarp();
+      if (lane == 0 && k - S >= 0) issue(k - S, stream);
+    });
+  }
+}
+
+template <typename T, int MODE>
+cudaError_t launch_fused_t(const CUtensorMap& map, const CastArgs& a, SinglePassWorkspace* ws, const LaunchCtx& ctx) {
+  auto fn = fused_kernel<T, MODE>;
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem_bytes<T>());
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit);
+  }
+  const int grid = a.num_tiles < ctx.num_sms ? a.num_tiles : ctx.num_sms;
+  if (grid == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = fused_smem_bytes<T>();
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (grid barrier)
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {(void*)&map, (void*)&a, (void*)&ws};
+  return cudaLaunchKernelExC(&cfg, (const void*)fn, args);
+}
+
+}  // namespace
+
+cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N);
+
+cudaError_t launch_single_pass(const void* x, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
+                               const LaunchCtx& ctx) {
+  CUtensorMap map;
+  cudaError_t e = make_x_tensor_map(&map, x, bf16, args.M, args.N);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles_m = (args.M + kTile - 1) / kTile, tiles_n = (args.N + kTile - 1) / kTile;
+  args.tiles_n = (int)tiles_n;
+  args.num_tiles = (int)(tiles_m * tiles_n);
+  if (bf16) {
+    if (mode == kCast1D) return launch_fused_t<uint16_t, kCast1D>(map, args, ws, ctx);
+    return launch_fused_t<uint16_t, kCast2D>(map, args, ws, ctx);
+  }
+  if (mode == kCast1D) return launch_fused_t<float, kCast1D>(map, args, ws, ctx);
+  return launch_fused_t<float, kCast2D>(map, args, ws, ctx);
+}
+
+}  // namespace nvfp4

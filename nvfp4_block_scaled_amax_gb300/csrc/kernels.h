@@ -66,6 +66,20 @@ struct CastArgs {
 // launched as a programmatic dependent of the preceding amax kernel.
 cudaError_t launch_cast(const void* x, bool bf16, int mode, CastArgs args, bool pdl, const LaunchCtx& ctx);
 
+// Scratch of the single-pass kernels (zeroed before first use, then kept
+// consistent by the kernels themselves): the grid barrier's arrival count
+// and generation, and the two alternating max accumulators.
+struct SinglePassWorkspace {
+  unsigned count;
+  unsigned gen;
+  unsigned acc[2];
+};
+
+// One persistent launch: per-tensor amax of x (written to args.amax_row /
+// args.amax_col) and the fused cast (1D or 2D), x read from HBM once.
+cudaError_t launch_single_pass(const void* x, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
+                               const LaunchCtx& ctx);
+
 // Row-scaled cast: per-row amax (unless skip_amax), row-wise codes/scales.
 cudaError_t launch_row_scaled(const void* x, bool bf16, int64_t M, int64_t N, uint8_t* data, uint8_t* scale,
                               float* amax, bool skip_amax, bool swizzled, const float* noop,

@@ -150,6 +150,41 @@ nvfp4_status quantize_per_tensor(int mode, const void* x, int dtype, int64_t M, 
   return from_cuda(launch_cast(x, bf16, mode, a, /*pdl=*/!skip, ctx));
 }
 
+nvfp4_status quantize_single_pass(int mode, const void* x, int dtype, int64_t M, int64_t N,
+                                  const nvfp4_output* out, unsigned flags, const float* noop, void* workspace,
+                                  void* stream) {
+  const unsigned allowed = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SWIZZLED;
+  nvfp4_status st = check_quantize(x, dtype, M, N, out, flags, allowed);
+  if (st != NVFP4_OK) return st;
+  if (mode == kCast2D && (M % 16 != 0 || N % 16 != 0)) return NVFP4_ERR_SHAPE;
+  if (workspace == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(workspace) || (noop != nullptr && !aligned16(noop))) return NVFP4_ERR_ALIGN;
+  LaunchCtx ctx;
+  if ((st = make_ctx(stream, &ctx)) != NVFP4_OK) return st;
+  const bool row = flags & NVFP4_ROWWISE, col = flags & NVFP4_COLWISE;
+  if (M == 0 || N == 0) {
+    // nothing to cast: the amax of an empty tensor is 0
+    return from_cuda(launch_amax(x, dtype == NVFP4_BF16, 0, row ? out->amax_row : out->amax_col,
+                                 row && col ? out->amax_col : nullptr, noop, ctx));
+  }
+  CastArgs a = {};
+  a.M = M;
+  a.N = N;
+  a.data_row = row ? out->data_row : nullptr;
+  a.scale_row = row ? out->scale_row : nullptr;
+  a.amax_row = row ? out->amax_row : nullptr;
+  a.data_col = col ? out->data_col : nullptr;
+  a.scale_col = col ? out->scale_col : nullptr;
+  a.amax_col = col ? out->amax_col : nullptr;
+  a.noop = noop;
+  a.status = ctx.status;
+  a.rowwise = row;
+  a.colwise = col;
+  a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
+  return from_cuda(launch_single_pass(x, dtype == NVFP4_BF16, mode, a,
+                                      static_cast<SinglePassWorkspace*>(workspace), ctx));
+}
+
 }  // namespace
 
 cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N) {
@@ -243,6 +278,18 @@ nvfp4_status nvfp4_quantize_2d(const void* x, int dtype, int64_t M, int64_t N, c
 nvfp4_status nvfp4_quantize_rht(const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,
                                 unsigned flags, uint32_t sign_mask, const float* noop, void* stream) {
   return quantize_per_tensor(kCastRHT, x, dtype, M, N, out, flags, sign_mask, noop, stream);
+}
+
+nvfp4_status nvfp4_quantize_1d_single_pass(const void* x, int dtype, int64_t M, int64_t N,
+                                           const nvfp4_output* out, unsigned flags, const float* noop,
+                                           void* workspace, void* stream) {
+  return quantize_single_pass(kCast1D, x, dtype, M, N, out, flags, noop, workspace, stream);
+}
+
+nvfp4_status nvfp4_quantize_2d_single_pass(const void* x, int dtype, int64_t M, int64_t N,
+                                           const nvfp4_output* out, unsigned flags, const float* noop,
+                                           void* workspace, void* stream) {
+  return quantize_single_pass(kCast2D, x, dtype, M, N, out, flags, noop, workspace, stream);
 }
 
 nvfp4_status nvfp4_quantize_row_scaled(const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,

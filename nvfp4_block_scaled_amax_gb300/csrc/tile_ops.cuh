@@ -1,0 +1,428 @@
+// tile_ops.cuh -- the per-tile arithmetic shared by the NVFP4 cast kernels:
+// a 128x128 tile of x staged by TMA in shared memory (128-byte swizzle) is
+// cast by 8 warps, each thread owning an 8x8 sub-block.
+//
+//   * a 1x16 row block is the sub-blocks of lanes l and l^1; a 16x1 column
+//     block those of lanes l and l^8; a 16x16 tile lanes l, l^1, l^8, l^9;
+//     block maxima are combined with one or two shuffles;
+//   * row-wise codes: one 32-bit word (8 codes) per row of the sub-block;
+//   * column-wise codes: one word per column of the sub-block, computed from
+//     the same registers (1D, with the column block's scale) or, in 2D, the
+//     8x8 nibble transpose of the row-wise words (same scale per tile);
+//   * the tile's scales are staged in shared memory ([128][8] bytes per
+//     direction) and stored as 16-byte lines of the cuBLAS 128x4 layout
+//     ("Fuse NVFP4 scale swizzling on SM120 and SM121", Changes: aligned
+//     groups of four scales written together) or 8-byte runs of the compact
+//     layout.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvfp4 {
+namespace tile {
+
+constexpr int kTile = 128;            // tile rows = tile columns (elements)
+constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 128 bytes
+
+template <typename T>
+struct TileCfg;
+template <>
+struct TileCfg<uint16_t> {
+  static constexpr int kBoxCols = 64, kBoxes = 2, kStages = 3, kMinBlocks = 2;
+};
+template <>
+struct TileCfg<float> {
+  static constexpr int kBoxCols = 32, kBoxes = 4, kStages = 3, kMinBlocks = 1;
+};
+
+template <typename T>
+__host__ __device__ constexpr int tile_bytes() {
+  return TileCfg<T>::kBoxes * kBoxBytes;
+}
+// stages | 2 encode-factor tables | 2 x 2 staged scale tiles | barriers | flag
+template <typename T>
+__host__ __device__ constexpr size_t smem_bytes() {
+  return 1024 + (size_t)TileCfg<T>::kStages * tile_bytes<T>() + 2 * 128 * 4 + 4 * 1024 +
+         8 * TileCfg<T>::kStages + 16;
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in box `box` of a
+// stage: the TMA 128-byte swizzle XORs the chunk index with row % 8.
+__device__ __forceinline__ uint32_t swz(int box, int row, int chunk) {
+  return (uint32_t)(box * kBoxBytes + row * 128 + (((chunk ^ row) & 7) << 4));
+}
+
+// E4M3 scale code of a block with maximum b under global scale g.
+__device__ __forceinline__ uint32_t block_scale(float b, float g) {
+  return e4m3_rn_satfinite(__fmul_rn(div6_rn(b), g));
+}
+
+// Two products in one packed FP32x2 multiply (each an IEEE product rounded
+// to nearest), then the E2M1 codes of eight values.
+__device__ __forceinline__ uint64_t mul2(float a, float b, uint64_t rr) {
+  uint64_t p, v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(a), "f"(b));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(v), "l"(rr));
+  return p;
+}
+__device__ __forceinline__ uint64_t splat2(float r) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(v) : "f"(r));
+  return v;
+}
+__device__ __forceinline__ uint32_t e2m1x8_pairs(uint64_t p0, uint64_t p1, uint64_t p2, uint64_t p3) {
+  uint32_t out;
+  asm("{\n"
+      ".reg .b8 q0, q1, q2, q3;\n"
+      ".reg .f32 a0, a1, a2, a3, a4, a5, a6, a7;\n"
+      "mov.b64 {a0, a1}, %1;\n"
+      "mov.b64 {a2, a3}, %2;\n"
+      "mov.b64 {a4, a5}, %3;\n"
+      "mov.b64 {a6, a7}, %4;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, a1, a0;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, a3, a2;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, a5, a4;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, a7, a6;\n"
+      "mov.b32 %0, {q0, q1, q2, q3};\n"
+      "}"
+      : "=r"(out)
+      : "l"(p0), "l"(p1), "l"(p2), "l"(p3));
+  return out;
+}
+// Codes of v[0..7] * r, v[0] in the low nibble.
+__device__ __forceinline__ uint32_t encode8(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                            float v7, float r) {
+  const uint64_t rr = splat2(r);
+  return e2m1x8_pairs(mul2(v0, v1, rr), mul2(v2, v3, rr), mul2(v4, v5, rr), mul2(v6, v7, rr));
+}
+
+// 8x8 transpose of 4-bit elements held as 8 words (word k = row k, element
+// c at bits 4c..4c+3): afterwards word c holds column c, row k at bits 4k.
+__device__ __forceinline__ void transpose_nibbles8x8(uint32_t (&w)[8]) {
+  // swap the off-diagonal elements of every 2x2 block of nibbles
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+    const uint32_t a = w[k], b = w[k + 1];
+    w[k] = (a & 0x0F0F0F0Fu) | ((b << 4) & 0xF0F0F0F0u);
+    w[k + 1] = ((a >> 4) & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u);
+  }
+  // then of every 2x2 block of bytes (2x2-nibble blocks)
+#pragma unroll
+  for (int k = 0; k < 8; k += 4) {
+#pragma unroll
+    for (int d = 0; d < 2; ++d) {
+      const uint32_t a = w[k + d], b = w[k + d + 2];
+      w[k + d] = __byte_perm(a, b, 0x6240);
+      w[k + d + 2] = __byte_perm(a, b, 0x7351);
+    }
+  }
+  // then of the 2x2 block of half-words (4x4-nibble blocks)
+#pragma unroll
+  for (int d = 0; d < 4; ++d) {
+    const uint32_t a = w[d], b = w[d + 4];
+    w[d] = __byte_perm(a, b, 0x5410);
+    w[d + 4] = __byte_perm(a, b, 0x7632);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 8x8 sub-block pass.  Warp w: bx = w & 1 (tile columns 64bx .. +63),
+// q = w >> 1 (tile rows 32q .. +31); lane l: j = l & 7 (columns 64bx + 8j ..
+// +7), i = l >> 3 (rows 32q + 8i .. +7).  For BF16 the eight lanes of one
+// shared-memory phase read eight different 16-byte chunks (conflict-free).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// Packed BF16 pair: per half max(|a|, |b|) (the sign bits are junk and are
+// cleared where the value is used).
+__device__ __forceinline__ uint32_t xsa(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// (lo of a, lo of b) and (hi of a, hi of b) -> per-half max of |.|: a packed
+// pair (max|a|, max|b|) from two packed pairs.
+__device__ __forceinline__ uint32_t xsa_pairs(uint32_t a, uint32_t b) {
+  return xsa(__byte_perm(a, b, 0x5410), __byte_perm(a, b, 0x7632));
+}
+
+// The 8x8 sub-block in registers.  BF16: w[k][p] holds columns 2p (low half)
+// and 2p+1 of row k.  FP32: w[k][c] is column c of row k.
+template <typename T>
+struct Sub {
+  static constexpr int kW = sizeof(T) == 2 ? 4 : 8;
+  uint32_t w[8][kW];
+  __device__ __forceinline__ float v(int k, int c) const {
+    if constexpr (sizeof(T) == 2)
+      return (c & 1) ? bf16_hi(w[k][c >> 1]) : bf16_lo(w[k][c >> 1]);
+    else
+      return __uint_as_float(w[k][c]);
+  }
+};
+
+// Loads rows trow..trow+7 of the sub-block; trow is a multiple of 8, so the
+// swizzled chunk of row trow + k is chunk ^ k, i.e. the address bits 4..6 of
+// the unswizzled address XOR k.
+template <typename T>
+__device__ __forceinline__ void load_sub(uint32_t stage, int bx, int trow, int j, Sub<T>& s) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t base = stage + bx * kBoxBytes + trow * 128 + (j << 4);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 c = lds128((base + 128 * k) ^ (k << 4));
+      s.w[k][0] = c.x; s.w[k][1] = c.y; s.w[k][2] = c.z; s.w[k][3] = c.w;
+    }
+  } else {
+    const uint32_t base = stage + (2 * bx + (j >> 2)) * kBoxBytes + trow * 128 + ((2 * (j & 3)) << 4);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 c0 = lds128((base + 128 * k) ^ (k << 4));
+      const uint4 c1 = lds128((base + 16 + 128 * k) ^ (k << 4));
+      s.w[k][0] = c0.x; s.w[k][1] = c0.y; s.w[k][2] = c0.z; s.w[k][3] = c0.w;
+      s.w[k][4] = c1.x; s.w[k][5] = c1.y; s.w[k][6] = c1.z; s.w[k][7] = c1.w;
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t encode_row(const Sub<T>& s, int k, float r) {
+  return encode8(s.v(k, 0), s.v(k, 1), s.v(k, 2), s.v(k, 3), s.v(k, 4), s.v(k, 5), s.v(k, 6), s.v(k, 7), r);
+}
+template <typename T>
+__device__ __forceinline__ uint32_t encode_col(const Sub<T>& s, int c, float r) {
+  return encode8(s.v(0, c), s.v(1, c), s.v(2, c), s.v(3, c), s.v(4, c), s.v(5, c), s.v(6, c), s.v(7, c), r);
+}
+
+// Packed pair (max|x| of row 2t, of row 2t+1) over the sub-block's columns,
+// combined with lane l^1 (the other half of each 1x16 block).  BF16 only.
+__device__ __forceinline__ uint32_t row_pair_max(const Sub<uint16_t>& s, int t) {
+  const uint32_t a = xsa(xsa(s.w[2 * t][0], s.w[2 * t][1]), xsa(s.w[2 * t][2], s.w[2 * t][3]));
+  const uint32_t b = xsa(xsa(s.w[2 * t + 1][0], s.w[2 * t + 1][1]), xsa(s.w[2 * t + 1][2], s.w[2 * t + 1][3]));
+  const uint32_t pr = xsa_pairs(a, b);
+  return xsa(pr, __shfl_xor_sync(0xFFFFFFFFu, pr, 1)) & 0x7FFF7FFFu;
+}
+// Packed pair (max|x| of column 2p, of column 2p+1) over the sub-block's 8
+// rows, combined with lane l^8 (the other half of each 16-row block).
+__device__ __forceinline__ uint32_t col_pair_max(const Sub<uint16_t>& s, int p) {
+  const uint32_t acc = xsa(xsa(xsa(s.w[0][p], s.w[1][p]), xsa(s.w[2][p], s.w[3][p])),
+                           xsa(xsa(s.w[4][p], s.w[5][p]), xsa(s.w[6][p], s.w[7][p])));
+  return xsa(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, 8)) & 0x7FFF7FFFu;
+}
+__device__ __forceinline__ float row_max_f32(const Sub<float>& s, int k) {
+  float m = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) m = fmaxf(m, fabsf(s.v(k, c)));
+  return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+}
+__device__ __forceinline__ float col_max_f32(const Sub<float>& s, int c) {
+  float m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(s.v(k, c)));
+  return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+}
+
+// 16x16 tile maximum: the sub-block's max combined over lanes l^1, l^8.
+template <typename T>
+__device__ __forceinline__ float tile_max(const Sub<T>& s) {
+  float m;
+  if constexpr (sizeof(T) == 2) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc = xsa(acc, xsa(xsa(s.w[k][0], s.w[k][1]), xsa(s.w[k][2], s.w[k][3])));
+    acc &= 0x7FFF7FFFu;
+    m = fmaxf(bf16_lo(acc), bf16_hi(acc));
+  } else {
+    m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) m = fmaxf(m, fabsf(s.v(k, c)));
+  }
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+}
+
+// Casts this thread's 8x8 sub-block of the staged tile at shared address
+// `stage`: stores its code words and stages its scales in the shared
+// buffers at sc_row ([128][8], by tile row) and sc_col ([128][8], by tile
+// column).  `warp` is the warp's index within the 8 warps casting the tile.
+// kDirs: 3 = both directions, 1 = row-wise only, 2 = column-wise only.
+// kInterior: the whole 128x128 tile lies inside x (no bounds checks).
+template <typename T, int MODE, int kDirs, bool kInterior>
+__device__ __forceinline__ void block_pass(uint32_t stage, const float* rtab_row, const float* rtab_col,
+                                           uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
+                                           int64_t c0, float g_row, float g_col, int warp) {
+  constexpr bool kRow = (kDirs & 1) != 0, kCol = (kDirs & 2) != 0;
+  const int lane = threadIdx.x & 31;
+  const int bx = warp & 1, q = warp >> 1, j = lane & 7, i = lane >> 3;
+  const int trow = 32 * q + 8 * i;   // first tile row of the sub-block
+  const int tcol = 64 * bx + 8 * j;  // first tile column
+  Sub<T> s;
+  load_sub<T>(stage, bx, trow, j, s);
+
+  // Output cursors: codes of row k at prow + k * srow, of column c at
+  // pcol + c * scol.  Outside x (edge tiles only) the stores are predicated
+  // off: bit k of row_ok / col_ok.
+  const int64_t M = a.M, N = a.N, y0 = r0 + trow, x0 = c0 + tcol;
+  const int64_t srow = N / 2, scol = M / 2;
+  uint8_t* prow = kRow ? a.data_row + y0 * srow + x0 / 2 : nullptr;
+  uint8_t* pcol = kCol ? a.data_col + x0 * scol + y0 / 2 : nullptr;
+  uint32_t row_ok = 0xFFu, col_ok = 0xFFu;
+  if (!kInterior) {
+    const int64_t rows_in = M - y0, cols_in = N - x0;
+    const uint32_t rk = rows_in >= 8 ? 0xFFu : (rows_in <= 0 ? 0u : (1u << rows_in) - 1u);
+    const uint32_t ck = cols_in >= 8 ? 0xFFu : (cols_in <= 0 ? 0u : (1u << cols_in) - 1u);
+    row_ok = cols_in > 0 ? rk : 0u;
+    col_ok = rows_in > 0 ? ck : 0u;
+  }
+  auto put_row = [&](int k, uint32_t w) {
+    if (kInterior)
+      st_cs_u32(prow, w);
+    else
+      st_cs_u32_if(prow, w, (row_ok >> k) & 1u);
+    prow += srow;
+  };
+  auto put_col = [&](int c, uint32_t w) {
+    if (kInterior)
+      st_cs_u32(pcol, w);
+    else
+      st_cs_u32_if(pcol, w, (col_ok >> c) & 1u);
+    pcol += scol;
+  };
+  const uint32_t srow_st = sc_row + trow * 8 + (tcol >> 4);  // staged row scales, one byte per row
+  const uint32_t scol_st = sc_col + tcol * 8 + (trow >> 4);  // staged column scales, one per column
+  const bool stage_row = (j & 1) == 0, stage_col = (i & 1) == 0;
+
+  if constexpr (MODE == kCast2D) {
+    const float m = tile_max<T>(s);
+    const uint32_t sr = block_scale(m, g_row);
+    const uint32_t sc = (g_col == g_row) ? sr : block_scale(m, g_col);
+    const float rr = rtab_row[sr], rc = rtab_col[sc];
+    uint32_t wc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t wr = encode_row<T>(s, k, kRow ? rr : rc);
+      if (kRow) put_row(k, wr);
+      if (kCol) wc[k] = (!kRow || rc == rr) ? wr : encode_row<T>(s, k, rc);
+    }
+    if (kCol) {
+      transpose_nibbles8x8(wc);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) put_col(c, wc[c]);
+    }
+    if (kRow && stage_row) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sts_u8(srow_st + 8 * k, sr);
+    }
+    if (kCol && stage_col) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) sts_u8(scol_st + 8 * c, sc);
+    }
+  } else {
+    // 1D: row blocks 1x16 (lanes l, l^1), column blocks 16x1 (lanes l, l^8).
+    if (kRow) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float m0, m1;
+        if constexpr (sizeof(T) == 2) {
+          const uint32_t pr = row_pair_max(s, t);
+          m0 = bf16_lo(pr);
+          m1 = bf16_hi(pr);
+        } else {
+          m0 = row_max_f32(s, 2 * t);
+          m1 = row_max_f32(s, 2 * t + 1);
+        }
+        const uint32_t s0 = block_scale(m0, g_row), s1 = block_scale(m1, g_row);
+        put_row(2 * t, encode_row<T>(s, 2 * t, rtab_row[s0]));
+        put_row(2 * t + 1, encode_row<T>(s, 2 * t + 1, rtab_row[s1]));
+        if (stage_row) {
+          sts_u8(srow_st + 16 * t, s0);
+          sts_u8(srow_st + 16 * t + 8, s1);
+        }
+      }
+    }
+    if (kCol) {
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        float m0, m1;
+        if constexpr (sizeof(T) == 2) {
+          const uint32_t pc = col_pair_max(s, p);
+          m0 = bf16_lo(pc);
+          m1 = bf16_hi(pc);
+        } else {
+          m0 = col_max_f32(s, 2 * p);
+          m1 = col_max_f32(s, 2 * p + 1);
+        }
+        const uint32_t s0 = block_scale(m0, g_col), s1 = block_scale(m1, g_col);
+        put_col(2 * p, encode_col<T>(s, 2 * p, rtab_col[s0]));
+        put_col(2 * p + 1, encode_col<T>(s, 2 * p + 1, rtab_col[s1]));
+        if (stage_col) {
+          sts_u8(scol_st + 16 * p, s0);
+          sts_u8(scol_st + 16 * p + 8, s1);
+        }
+      }
+    }
+  }
+}
+
+// block_pass for the directions and tile position at hand.
+template <typename T, int MODE>
+__device__ __forceinline__ void block_pass_any(uint32_t stage, const float* rtab_row, const float* rtab_col,
+                                               uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
+                                               int64_t c0, float g_row, float g_col, bool do_row, bool do_col,
+                                               int warp) {
+  const bool interior = (r0 + kTile <= a.M) && (c0 + kTile <= a.N);
+  if (do_row && do_col) {
+    if (interior)
+      block_pass<T, MODE, 3, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+    else
+      block_pass<T, MODE, 3, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+  } else if (do_row) {
+    if (interior)
+      block_pass<T, MODE, 1, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+    else
+      block_pass<T, MODE, 1, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+  } else if (do_col) {
+    if (interior)
+      block_pass<T, MODE, 2, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+    else
+      block_pass<T, MODE, 2, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+  }
+}
+
+// Stores one direction's staged scale tile [128 rows][8 scale columns] at
+// rows R0.., scale columns C0.. of an R x C scale matrix; t = 0..127.
+__device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out, int64_t R0, int64_t C0, int64_t R,
+                                                 int64_t C, bool swizzled, int t) {
+  if (swizzled) {
+    // Two 512-byte tiles of the 128x4 layout, contiguous (R, C aligned):
+    // 16-byte line L of tile h holds rows L, L+32, L+64, L+96, 4 scales each.
+    if (t >= 64) return;
+    const int h = t >> 5, L = t & 31;
+    uint32_t w[4];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) w[qq] = *reinterpret_cast<const uint32_t*>(s + (32 * qq + L) * 8 + 4 * h);
+    uint8_t* base = out + ((R0 >> 7) * (C >> 2) + (C0 >> 2) + h) * 512 + L * 16;
+    st_cs_v4(base, w[0], w[1], w[2], w[3]);
+  } else {
+    const int64_t r = R0 + t;
+    if (r >= R) return;
+    const int64_t n = (C - C0) < 8 ? (C - C0) : 8;
+    if (n <= 0) return;
+    uint8_t* p = out + r * C + C0;
+    const uint2 v = *reinterpret_cast<const uint2*>(s + t * 8);
+    if (n == 8 && (reinterpret_cast<uintptr_t>(p) & 7) == 0) {
+      st_cs_v2(p, v.x, v.y);
+    } else {
+      for (int b = 0; b < n; ++b) st_cs_u8(p + b, (b < 4 ? v.x : v.y) >> (8 * (b & 3)));
+    }
+  }
+}
+
+}  // namespace tile
+}  // namespace nvfp4

@@ -99,6 +99,16 @@ def test_quantize_validation(lib):
     assert lib.nvfp4_quantize_row_scaled(X, 0, 256, 256, ctypes.byref(o), COL, None, None) == ERR_FLAGS
 
 
+def test_single_pass_validation(lib):
+    o = out(lib)
+    for fn in (lib.nvfp4_quantize_1d_single_pass, lib.nvfp4_quantize_2d_single_pass):
+        assert fn(X, 0, 256, 256, ctypes.byref(o), ROW | COL, None, None, None) == ERR_NULL        # workspace
+        assert fn(X, 0, 256, 256, ctypes.byref(o), ROW | COL, None, A + 4, None) == ERR_ALIGN
+        assert fn(X, 0, 256, 256, ctypes.byref(o), ROW | SKIP, None, A, None) == ERR_FLAGS        # no skip-amax
+        assert fn(X, 0, 192, 256, ctypes.byref(o), ROW | COL | SWZ, None, A, None) == ERR_ALIGN
+    assert lib.nvfp4_quantize_2d_single_pass(X, 0, 24, 256, ctypes.byref(o), ROW, None, A, None) == ERR_SHAPE
+
+
 def test_amax_and_misc_validation(lib):
     assert lib.nvfp4_compute_amax(X, 0, 16, 16, None, None, None, None) == ERR_NULL
     assert lib.nvfp4_compute_amax(X, 0, 16, 16, C, C, None, None) == ERR_FLAGS

@@ -33,17 +33,37 @@ def _flags():
 @pytest.mark.parametrize("M,N", SHAPES)
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("mode", ["1d", "2d"])
-def test_quantize_matches_oracle(oracle_mod, M, N, dtype, mode):
+@pytest.mark.parametrize("path", ["two_pass", "single_pass"])
+def test_quantize_matches_oracle(oracle_mod, M, N, dtype, mode, path):
     x = _x(M, N, dtype, seed=M * 7 + N, kind="outliers")
     xd = x.cuda()
     swz_ok = M % 128 == 0 and N % 128 == 0
     for rowwise, colwise in _flags():
         ref = oracle_mod.quantize(mode, bits(x), rowwise=rowwise, colwise=colwise)
         for swizzled in ([False, True] if swz_ok else [False]):
-            q = nv.quantize(xd, mode, rowwise=rowwise, colwise=colwise, swizzled=swizzled)
+            q = nv.quantize(xd, mode, rowwise=rowwise, colwise=colwise, swizzled=swizzled, path=path)
             torch.cuda.synchronize()
             assert_quantize_equal(oracle_mod, q, ref, swizzled, rowwise, colwise,
-                                  what=f"{mode} {M}x{N} {dtype} r{rowwise}c{colwise}s{swizzled}")
+                                  what=f"{mode} {path} {M}x{N} {dtype} r{rowwise}c{colwise}s{swizzled}")
+
+
+@pytest.mark.parametrize("mode", ["1d", "2d"])
+def test_single_pass_workspace_reuse(oracle_mod, mode):
+    """The grid barrier's generation counter keeps one workspace valid over
+    many calls of different grid sizes (tile counts), and across the
+    dual-amax reuse sequence."""
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    for it, (M, N) in enumerate([(128, 128), (1024, 2048), (256, 384), (2048, 2048), (16, 16)] * 3):
+        base = _x(M, N, torch.bfloat16, seed=it, kind="outliers")
+        for x in inputs.reuse_sequence(base):
+            q = nv.quantize(x.cuda(), mode, path="single_pass", workspace=ws)
+            torch.cuda.synchronize()
+            ref = oracle_mod.quantize(mode, bits(x))
+            assert_quantize_equal(oracle_mod, q, ref, False, what=f"{mode} {M}x{N} call {it}")
+    w = ws.view(torch.int32).cpu()
+    assert int(w[0]) == 0                       # arrival count back to zero
+    assert int(w[1]) == 15 * 4                  # one generation per call
+    assert nv.device_status() == 0
 
 
 @pytest.mark.parametrize("M,N", [(16, 16), (128, 128), (48, 80), (208, 336), (384, 640), (1088, 1024)])
@@ -95,7 +115,8 @@ def test_empty_inputs():
         assert q.amax_row.item() == 0.0 and q.amax_col.item() == 0.0
 
 
-def test_dual_amax_refreshed_on_reuse(oracle_mod):
+@pytest.mark.parametrize("path", ["two_pass", "single_pass"])
+def test_dual_amax_refreshed_on_reuse(oracle_mod, path):
     """'Write both NVFP4 amax buffers', Changes: one output reused over
     inputs whose maximum decreases, reaches zero and rises again."""
     for mode, dtype, (M, N) in [("1d", torch.bfloat16, (256, 256)), ("2d", torch.float32, (128, 384)),
@@ -104,7 +125,7 @@ def test_dual_amax_refreshed_on_reuse(oracle_mod):
         for rowwise, colwise in _flags():
             q = nv.empty(M, N, rowwise, colwise, device="cuda")
             for x in inputs.reuse_sequence(base) + [base * 0.0]:
-                nv.quantize(x.cuda(), mode, rowwise=rowwise, colwise=colwise, out=q)
+                nv.quantize(x.cuda(), mode, rowwise=rowwise, colwise=colwise, out=q, path=path)
                 torch.cuda.synchronize()
                 a = oracle_mod.amax(bits(x))
                 if rowwise:
@@ -141,7 +162,8 @@ def test_compute_amax_rht_matches_oracle(oracle_mod):
         assert b.item() == oracle_mod.rht_amax(bits(x), mask)
 
 
-def test_noop_leaves_everything_untouched():
+@pytest.mark.parametrize("path", ["two_pass", "auto"])
+def test_noop_leaves_everything_untouched(path):
     M, N = 256, 256
     x = _x(M, N, torch.bfloat16, seed=2).cuda()
     for mode in ("1d", "2d", "rht", "row_scaled"):
@@ -153,7 +175,7 @@ def test_noop_leaves_everything_untouched():
             if t is not None:
                 t.fill_(-3.0)
         noop = torch.ones(1, device="cuda")
-        nv.quantize(x, mode, out=q, noop=noop, sign_mask=0x1234)
+        nv.quantize(x, mode, out=q, noop=noop, sign_mask=0x1234, path=path if mode in ("1d", "2d") else "auto")
         torch.cuda.synchronize()
         for t in (q.data_row, q.scale_row, q.data_col, q.scale_col):
             if t is not None:
@@ -162,7 +184,7 @@ def test_noop_leaves_everything_untouched():
             if t is not None:
                 assert bool((t == -3.0).all())
         noop.zero_()
-        nv.quantize(x, mode, out=q, noop=noop, sign_mask=0x1234)
+        nv.quantize(x, mode, out=q, noop=noop, sign_mask=0x1234, path=path if mode in ("1d", "2d") else "auto")
         torch.cuda.synchronize()
         assert q.amax_row[0].item() > 0
 
