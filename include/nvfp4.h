@@ -176,13 +176,15 @@ nvfp4_status nvfp4_quantize_rht(const void* x, int dtype, int64_t M, int64_t N,
  * directly in the GEMM layout.)
  *   workspace: NVFP4_SINGLE_PASS_WORKSPACE_BYTES of device memory, zeroed
  *   before its first use and not shared by calls that can run at the same
- *   time; the kernel leaves it ready for the next call.  After a call that
- *   reported NVFP4_ERR_TIMEOUT through nvfp4_device_status, zero it again.
+ *   time; the kernel leaves it ready for the next call (it holds a barrier
+ *   generation, two arrival counts and one 4-byte partial maximum per CTA,
+ *   one CTA per SM: up to 1008 SMs).  After a call that reported
+ *   NVFP4_ERR_TIMEOUT through nvfp4_device_status, zero it again.
  *   flags: ROWWISE | COLWISE | SWIZZLED (no SKIP_AMAX: use the two-pass
  *   entry points for a given amax).  All CTAs must be co-resident (one per
  *   SM); a device where that is impossible returns NVFP4_ERR_CUDA.
  */
-#define NVFP4_SINGLE_PASS_WORKSPACE_BYTES 256
+#define NVFP4_SINGLE_PASS_WORKSPACE_BYTES 4096
 nvfp4_status nvfp4_quantize_1d_single_pass(const void* x, int dtype, int64_t M, int64_t N,
                                            const nvfp4_output* out, unsigned flags, const float* noop,
                                            void* workspace, void* stream);

@@ -182,7 +182,7 @@ def quantize(x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: b
 
     path: "auto" | "single_pass" | "two_pass" (1d / 2d only; see the module
     docstring).  workspace: for the single-pass path, a zeroed uint8 CUDA
-    tensor of at least 256 bytes owned by the caller (default: one cached
+    tensor of at least 4096 bytes owned by the caller (default: one cached
     per device and stream)."""
     if x.dim() != 2:
         raise ValueError("x must be 2-D (M x N)")

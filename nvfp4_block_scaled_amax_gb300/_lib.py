@@ -22,7 +22,7 @@ EXPORTS = ("nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_compute_amax", "nv
            "nvfp4_quantize_1d", "nvfp4_quantize_2d", "nvfp4_quantize_row_scaled", "nvfp4_quantize_rht",
            "nvfp4_quantize_1d_single_pass", "nvfp4_quantize_2d_single_pass",
            "nvfp4_dequantize", "nvfp4_swizzle_scales", "nvfp4_device_status")
-SINGLE_PASS_WORKSPACE_BYTES = 256
+SINGLE_PASS_WORKSPACE_BYTES = 4096
 
 
 class Output(ctypes.Structure):

@@ -89,33 +89,57 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
-// Grid-wide maximum of one non-negative float per CTA (called by one thread
-// per CTA).  Generation-counted so the workspace needs no clearing between
-// calls: call g accumulates into acc[g & 1]; its last arriver resets the
-// arrival count and acc[(g + 1) & 1] for the next call, then publishes
-// g + 1.  The spin is bounded; false means it ran out.
-__device__ bool grid_max(SinglePassWorkspace* ws, float m, unsigned n_cta, unsigned* status, float* out) {
-  const unsigned gen = ld_acquire_gpu(&ws->gen);
-  atomicMax(&ws->acc[gen & 1u], __float_as_uint(m));
-  __threadfence();
-  const unsigned arrived = atomicAdd(&ws->count, 1u);
-  if (arrived == n_cta - 1) {
-    atomicExch(&ws->count, 0u);
-    atomicExch(&ws->acc[(gen + 1u) & 1u], 0u);
-    __threadfence();
-    atomicExch(&ws->gen, gen + 1u);
-  } else {
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_add_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide maximum of one non-negative float per CTA, called by all threads
+// of every CTA.  Generation-counted, so the workspace needs no clearing
+// between calls: call g (read from ws->gen at the start) publishes its CTA
+// maxima in ws->slot[] and arrives on ws->count[g & 1]; every CTA polls the
+// count (bounded) and reduces the slots itself.  CTA 0 clears the other
+// count, which the next call uses, and advances the generation, which the
+// next call (ordered after this kernel) reads.  Returns false when the wait
+// ran out.  `red` is 32 floats of shared memory.
+__device__ bool grid_max(SinglePassWorkspace* ws, float m, unsigned n_cta, unsigned* status, float* red,
+                         float* out) {
+  __shared__ unsigned s_ok;
+  const unsigned tid = threadIdx.x;
+  if (tid == 0) {
+    const unsigned gen = ld_acquire_gpu(&ws->gen);
+    st_release_gpu(&ws->slot[blockIdx.x], __float_as_uint(m));
+    red_release_add_gpu(&ws->count[gen & 1u], 1u);
+    bool ok = true;
     const long long t0 = clock64();
-    while (ld_acquire_gpu(&ws->gen) == gen) {
+    while (ld_acquire_gpu(&ws->count[gen & 1u]) < n_cta) {
       if (clock64() - t0 > kWaitLimitCycles) {
         atomicOr(status, kStatusGridTimeout);
-        return false;
+        ok = false;
+        break;
       }
-      __nanosleep(64);
     }
+    if (blockIdx.x == 0 && ok) {
+      ws->count[(gen + 1u) & 1u] = 0u;  // unused by this call; the next one counts there
+      st_release_gpu(&ws->gen, gen + 1u);
+    }
+    s_ok = ok ? 1u : 0u;
   }
-  __threadfence();
-  *out = __uint_as_float(atomicAdd(&ws->acc[gen & 1u], 0u));
+  __syncthreads();
+  if (!s_ok) return false;
+  float v = 0.0f;
+  for (unsigned c = tid; c < n_cta; c += blockDim.x) v = fmaxf(v, __uint_as_float(ld_acquire_gpu(&ws->slot[c])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if ((tid & 31) == 0) red[tid >> 5] = v;
+  __syncthreads();
+  if (tid == 0) {
+    float r = 0.0f;
+    for (unsigned w = 0; w < (blockDim.x >> 5); ++w) r = fmaxf(r, red[w]);
+    *out = r;
+  }
   return true;
 }
 
@@ -244,17 +268,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   if (tid == 0) {
     float cm = 0.0f;
     for (int w = 0; w < kWarps; ++w) cm = fmaxf(cm, sm.red[w]);
-    float amax = 0.0f;
-    // A CTA that lost a wait still arrives, so the others are not held up.
-    const bool gok = grid_max(ws, cm, (unsigned)G, a.status, &amax);
+    sm.red[32] = cm;
+  }
+  __syncthreads();
+  // A CTA that lost a wait still arrives, so the others are not held up.
+  const bool gok = grid_max(ws, sm.red[32], (unsigned)G, a.status, sm.red, sm.amax);
+  if (tid == 0) {
     if (!gok) *sm.abort_flag = 1;
-    *sm.amax = amax;
+    const float amax = *sm.amax;
     if (b == 0 && gok && !*sm.abort_flag) {
       if (a.amax_row) *const_cast<float*>(a.amax_row) = amax;
       if (a.amax_col) *const_cast<float*>(a.amax_col) = amax;
     }
-    const float g = global_encode_scale(amax);
-    *sm.amax = g;
+    *sm.amax = global_encode_scale(amax);
   }
   __syncthreads();
   if (*sm.abort_flag) {
@@ -327,6 +353,11 @@ cudaError_t launch_fused_t(const CUtensorMap& map, const CastArgs& a, SinglePass
 }  // namespace
 
 cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N);
+
+int single_pass_grid(int64_t M, int64_t N, const LaunchCtx& ctx) {
+  const int64_t tiles = ((M + kTile - 1) / kTile) * ((N + kTile - 1) / kTile);
+  return (int)(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+}
 
 cudaError_t launch_single_pass(const void* x, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
                                const LaunchCtx& ctx) {

@@ -67,18 +67,25 @@ struct CastArgs {
 cudaError_t launch_cast(const void* x, bool bf16, int mode, CastArgs args, bool pdl, const LaunchCtx& ctx);
 
 // Scratch of the single-pass kernels (zeroed before first use, then kept
-// consistent by the kernels themselves): the grid barrier's arrival count
-// and generation, and the two alternating max accumulators.
+// consistent by the kernels themselves): the grid barrier's generation, the
+// arrival counts of the two alternating generations, and one partial
+// maximum per CTA.
 struct SinglePassWorkspace {
-  unsigned count;
   unsigned gen;
-  unsigned acc[2];
+  unsigned count[2];
+  unsigned pad[13];
+  unsigned slot[1];  // [grid]
 };
+constexpr size_t kSinglePassHeaderBytes = 64;
+// Most CTAs a workspace of `bytes` bytes can serve.
+constexpr int single_pass_max_ctas(size_t bytes) { return (int)((bytes - kSinglePassHeaderBytes) / 4); }
 
 // One persistent launch: per-tensor amax of x (written to args.amax_row /
 // args.amax_col) and the fused cast (1D or 2D), x read from HBM once.
 cudaError_t launch_single_pass(const void* x, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
                                const LaunchCtx& ctx);
+// CTAs the single-pass kernel uses for an M x N input.
+int single_pass_grid(int64_t M, int64_t N, const LaunchCtx& ctx);
 
 // Row-scaled cast: per-row amax (unless skip_amax), row-wise codes/scales.
 cudaError_t launch_row_scaled(const void* x, bool bf16, int64_t M, int64_t N, uint8_t* data, uint8_t* scale,
