@@ -193,6 +193,33 @@ nvfp4_status nvfp4_quantize_2d_single_pass(const void* x, int dtype, int64_t M, 
                                            void* workspace, void* stream);
 
 /*
+ * nvfp4_quantize_2d_single_pass for callers that cannot allocate device
+ * memory.  This entry point has no counterpart on the pages this library
+ * follows.  It computes exactly what nvfp4_quantize_2d_single_pass computes,
+ * but takes no workspace: its scratch is a 1024-byte array inside the
+ * library that the CUDA runtime places on every GPU that loads it (held
+ * until the process exits).  It serves callers with no device allocator of
+ * their own (a plain C host embedding the library), callers on paths that
+ * must not take an allocator's lock or risk a synchronizing cudaMalloc or
+ * cudaFree, and processes that size all device memory up front.
+ *   * The first call on a device looks up the array's device address (a
+ *     runtime query, no allocation); make that first call before any stream
+ *     capture on that device.
+ *   * Every call clears the array's barrier header on `stream` (a memset)
+ *     and then launches the kernel; it calls no cudaMalloc / cudaFree.
+ *   * All calls on a device share the one array: calls that can overlap on
+ *     the GPU (other streams, other threads) race and give wrong results;
+ *     serialize them.
+ *   * Limit: the kernel uses one CTA per SM, min(SMs, 128x128 tiles of x);
+ *     the array holds one partial maximum for up to 240 CTAs.  A launch
+ *     that would need more returns NVFP4_ERR_SHAPE (no GB300 does).
+ * Arguments, flags and errors otherwise as nvfp4_quantize_2d_single_pass.
+ */
+nvfp4_status nvfp4_quantize_2d_single_pass_noalloc(const void* x, int dtype, int64_t M, int64_t N,
+                                                   const nvfp4_output* out, unsigned flags,
+                                                   const float* noop, void* stream);
+
+/*
  * Dequantize one direction of an NVFP4 tensor ("Implement row-scaled NVFP4
  * fprop recipe", Important Files Changed, dequantize_nvfp4.cuh: row y uses
  * tensor_amax[y] when row-scaled, else tensor_amax[0]):

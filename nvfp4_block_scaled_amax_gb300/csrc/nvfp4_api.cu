@@ -188,6 +188,17 @@ nvfp4_status quantize_single_pass(int mode, const void* x, int dtype, int64_t M,
 
 }  // namespace
 
+// The host-side checks of the single-pass entry points (everything before
+// the launch), for callers that supply their own scratch.
+nvfp4_status validate_single_pass(int mode, const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,
+                                  unsigned flags, const float* noop) {
+  nvfp4_status st = check_quantize(x, dtype, M, N, out, flags, NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SWIZZLED);
+  if (st != NVFP4_OK) return st;
+  if (mode == kCast2D && (M % 16 != 0 || N % 16 != 0)) return NVFP4_ERR_SHAPE;
+  if (noop != nullptr && !aligned16(noop)) return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
 cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
