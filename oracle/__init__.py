@@ -36,7 +36,13 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-s
 
 
 def build(force: bool = False) -> str:
-    """Compiles the oracle with gcc (no SIMD intrinsics, no FMA contraction)."""
+    """Compiles the oracle with gcc (no SIMD intrinsics, no FMA contraction).
+
+    ``NVFP4_ORACLE_LIB`` names an already built copy to load instead; the
+    planted-mistake tests use it to run the pins against altered copies."""
+    override = os.environ.get("NVFP4_ORACLE_LIB")
+    if override:
+        return override
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
         subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])

@@ -235,6 +235,32 @@ def test_block_holding_the_maximum_gets_scale_448(oracle_mod):
         assert oracle_mod.block_scale(a, oracle_mod.global_encode_scale(a)) == 0x7E
 
 
+def test_block_scale_divides_by_6_before_multiplying(oracle_mod):
+    """Reading of the scale formula block_amax / 6 * global_enc: the FP32
+    quotient first, then the product.  Random inputs rarely tell the two FP32
+    orders apart, so the cases are built next to E4M3 rounding midpoints
+    (block maxima a few ulps around 6*m/g) and kept where (b/6)*g and (b*g)/6
+    round to different scales; numpy FP32 arithmetic and PyTorch's E4M3 cast
+    give the expected scale."""
+    rng = np.random.default_rng(12)
+    codes = np.arange(0x08, 0x7E, dtype=np.uint8)
+    lo, hi = np_e4m3_value(codes), np_e4m3_value(codes + 1)
+    mid = ((lo.astype(np.float64) + hi) / 2)
+    g = (np.float32(2688.0) / rng.uniform(0.1, 100.0, mid.size * 64).astype(np.float32)).astype(np.float32)
+    m = np.repeat(mid, 64)
+    b0 = (6.0 * m / g.astype(np.float64)).astype(np.float32)
+    cases = []
+    for d in range(-3, 4):
+        b = (b0.view(np.int32) + d).view(np.float32)
+        first = np_e4m3((b / np.float32(6.0)) * g)
+        other = np_e4m3((b * g) / np.float32(6.0))
+        sel = np.nonzero(first != other)[0]
+        cases += [(b[i], g[i], first[i]) for i in sel]
+    assert len(cases) >= 50
+    for b, g_, s in cases[:400]:
+        assert oracle_mod.block_scale(float(b), float(g_)) == s
+
+
 def test_global_scale_closed_forms(oracle_mod):
     assert oracle_mod.global_encode_scale(0.0) == 1.0
     assert oracle_mod.global_encode_scale(2688.0) == 1.0
