@@ -47,7 +47,9 @@ struct Smem {
 template <typename T>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
   Smem s;
-  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023);
+  // offset arithmetic on the shared array itself, so that every carved
+  // pointer stays a known shared-memory pointer (ld.shared / atom.shared)
+  uint8_t* p = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
   s.stages = p;
   p += (size_t)TileCfg<T>::kStages * tile_bytes<T>();
   s.rtab_row = reinterpret_cast<float*>(p);

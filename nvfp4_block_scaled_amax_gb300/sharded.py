@@ -94,12 +94,12 @@ class CudaBackend:
     """The library's kernels on the slab's GPU."""
 
     def local_amax(self, x: torch.Tensor, mode: str, sign_mask: int) -> torch.Tensor:
-        a = torch.zeros(2, dtype=torch.float32, device=x.device)
+        a = torch.zeros(8, dtype=torch.float32, device=x.device)  # two 16-byte aligned slots
         if mode == "rht":
-            compute_amax_rht(x, sign_mask, a[0:1], a[1:2])
+            compute_amax_rht(x, sign_mask, a[0:1], a[4:5])
         else:
-            compute_amax(x, a[0:1], a[1:2])
-        return a
+            compute_amax(x, a[0:1], a[4:5])
+        return a[0::4]
 
     def cast(self, x: torch.Tensor, mode: str, amax: torch.Tensor, rowwise: bool, colwise: bool,
              swizzled: bool, sign_mask: int) -> NVFP4Tensor:
