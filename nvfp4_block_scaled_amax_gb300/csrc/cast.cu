@@ -38,8 +38,8 @@ struct Smem {
   uint8_t* stages;
   float* rtab_row;  // [128] encode factor per E4M3 code, row-wise g
   float* rtab_col;  // [128] same, column-wise g
-  uint8_t* sc_row;  // [2][128][8] staged row-wise scales of a tile (by tile parity)
-  uint8_t* sc_col;  // [2][128][8] staged column-wise scales
+  uint8_t* sc_row;  // [2][kScRegion] staged row-wise scales of a tile (by tile parity)
+  uint8_t* sc_col;  // [2][kScRegion] staged column-wise scales
   uint64_t* bars;   // [kStages]
   int* abort_flag;
 };
@@ -55,8 +55,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.rtab_row = reinterpret_cast<float*>(p);
   s.rtab_col = s.rtab_row + 128;
   s.sc_row = reinterpret_cast<uint8_t*>(s.rtab_col + 128);
-  s.sc_col = s.sc_row + 2048;
-  s.bars = reinterpret_cast<uint64_t*>(s.sc_col + 2048);
+  s.sc_col = s.sc_row + 2 * kScRegion;
+  s.bars = reinterpret_cast<uint64_t*>(s.sc_col + 2 * kScRegion);
   s.abort_flag = reinterpret_cast<int*>(s.bars + TileCfg<T>::kStages);
   return s;
 }
@@ -103,7 +103,7 @@ __device__ __forceinline__ void rht_col_pass(const uint8_t* st, const Smem& sm, 
       const float rf = sm.rtab_col[s];
       code[2 * blk] = encode8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], rf);
       code[2 * blk + 1] = encode8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15], rf);
-      sm.sc_col[parity * 1024 + tcol * 8 + (rbase >> 4) + blk] = (uint8_t)s;
+      sm.sc_col[parity * kScRegion + ((rbase >> 4) + blk) * kScPitchCol + tcol] = (uint8_t)s;
     }
     // M % 16 == 0: the first block is inside when rg < M, the second when
     // rg + 16 < M.
@@ -183,8 +183,8 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
     const uint8_t* st = sm.stages + (size_t)s * tile_bytes<T>();
     const int parity = k & 1;
     if (ok && (do_row || do_col_blk))
-      block_pass_any<T, MODE>(smem_u32(st), sm.rtab_row, sm.rtab_col, smem_u32(sm.sc_row + parity * 1024),
-                              smem_u32(sm.sc_col + parity * 1024), a, r0, c0, g_row, g_col, do_row, do_col_blk,
+      block_pass_any<T, MODE>(smem_u32(st), sm.rtab_row, sm.rtab_col, smem_u32(sm.sc_row + parity * kScRegion),
+                              smem_u32(sm.sc_col + parity * kScRegion), a, r0, c0, g_row, g_col, do_row, do_col_blk,
                               threadIdx.x >> 5);
     if constexpr (MODE == kCastRHT) {
       if (ok && a.colwise) rht_col_pass(st, sm, a, r0, c0, g_col, sgn, parity);
@@ -195,9 +195,11 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
     // this tile's scales: threads 0..127 row-wise, 128..255 column-wise
     if (tid < 128) {
       if (do_row)
-        store_scale_tile(sm.sc_row + parity * 1024, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, tid);
+        store_scale_tile<MODE, false>(sm.sc_row + parity * kScRegion, a.scale_row, r0, c0 / 16, a.M, a.N / 16,
+                                      a.swizzled, tid);
     } else if (a.colwise) {
-      store_scale_tile(sm.sc_col + parity * 1024, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, tid - 128);
+      store_scale_tile<MODE, true>(sm.sc_col + parity * kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16,
+                                   a.swizzled, tid - 128);
     }
   }
   if (k < my_count && tid == 0) {

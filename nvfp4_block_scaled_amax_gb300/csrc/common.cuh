@@ -230,6 +230,9 @@ __device__ __forceinline__ void st_cs_u32_if(void* p, uint32_t a, uint32_t pred)
 __device__ __forceinline__ void sts_u8(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void sts_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
 __device__ __forceinline__ void st_cs_u16(void* p, uint32_t a) {
   asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(a)) : "memory");
 }

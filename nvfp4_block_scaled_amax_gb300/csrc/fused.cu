@@ -46,13 +46,13 @@ struct FusedCfg<float> {
 
 template <typename T>
 __host__ __device__ constexpr size_t fused_smem_bytes() {
-  return 1024 + (size_t)FusedCfg<T>::kStages * (tile_bytes<T>() + 2048) + 2 * 128 * 4 +
+  return 1024 + (size_t)FusedCfg<T>::kStages * (tile_bytes<T>() + 2 * kScRegion) + 2 * 128 * 4 +
          16 * FusedCfg<T>::kStages + 64 * 4 + 64;
 }
 
 struct FSmem {
   uint8_t* stages;   // [S][tile]
-  uint8_t* sc;       // [S][2][1024] staged row / column scales of the tile in stage s
+  uint8_t* sc;       // [S][2][kScRegion] staged row / column scales of the tile in stage s
   float* rtab_row;   // [128]
   float* rtab_col;   // [128]
   uint64_t* full;    // [S]
@@ -73,7 +73,7 @@ __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
   s.stages = p;
   p += (size_t)S * tile_bytes<T>();
   s.sc = p;
-  p += (size_t)S * 2048;
+  p += (size_t)S * 2 * kScRegion;
   s.rtab_row = reinterpret_cast<float*>(p);
   s.rtab_col = s.rtab_row + 128;
   s.full = reinterpret_cast<uint64_t*>(s.rtab_col + 128);
@@ -309,13 +309,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if (k < kept_from && !wait_full(s)) return;  // the waiting CTA gives up; outputs unfinished
     int64_t r0, c0;
     tile_rc(k, r0, c0);
-    uint8_t* sc = sm.sc + (size_t)s * 2048;
+    uint8_t* sc = sm.sc + (size_t)s * 2 * kScRegion;
     block_pass_any<T, MODE>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), sm.rtab_row, sm.rtab_col,
-                            smem_u32(sc), smem_u32(sc + 1024), a, r0, c0, g, g, do_row, do_col, cw);
+                            smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, g, do_row, do_col, cw);
     finish_stage(s, [&] {
       for (int t = lane; t < 128; t += 32) {
-        if (do_row) store_scale_tile(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
-        if (do_col) store_scale_tile(sc + 1024, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
+        if (do_row) store_scale_tile<MODE, false>(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
+        if (do_col)
+          store_scale_tile<MODE, true>(sc + kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
       }
       __syncwarp();
       if (lane == 0 && k - S >= 0) issue(k - S, stream);

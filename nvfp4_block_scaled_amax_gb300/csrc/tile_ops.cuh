@@ -9,11 +9,10 @@
 //   * column-wise codes: one word per column of the sub-block, computed from
 //     the same registers (1D, with the column block's scale) or, in 2D, the
 //     8x8 nibble transpose of the row-wise words (same scale per tile);
-//   * the tile's scales are staged in shared memory ([128][8] bytes per
-//     direction) and stored as 16-byte lines of the cuBLAS 128x4 layout
-//     ("Fuse NVFP4 scale swizzling on SM120 and SM121", Changes: aligned
-//     groups of four scales written together) or 8-byte runs of the compact
-//     layout.
+//   * the tile's scales are staged in shared memory (see staged_scale) and
+//     stored as 16-byte lines of the cuBLAS 128x4 layout ("Fuse NVFP4 scale
+//     swizzling on SM120 and SM121", Changes: aligned groups of four scales
+//     written together) or 8-byte runs of the compact layout.
 #pragma once
 
 #include "common.cuh"
@@ -40,10 +39,30 @@ template <typename T>
 __host__ __device__ constexpr int tile_bytes() {
   return TileCfg<T>::kBoxes * kBoxBytes;
 }
-// stages | 2 encode-factor tables | 2 x 2 staged scale tiles | barriers | flag
+// Staged scales of one tile, one region per direction.  Index r is the tile
+// row of that direction's output (an x row for the row-wise scales, an x
+// column for the column-wise ones), c its scale column (0..7).
+//   * 1D: scale (r, c) at c * pitch + r.  A thread stages the eight scales of
+//     its sub-block's rows (row-wise) or columns (column-wise) for one scale
+//     column with one 8-byte store; the pitches (row-wise 160, column-wise
+//     192 bytes) put the eight-byte stores of a warp in distinct banks.
+//   * 2D: one byte per 16x16 tile, at (r / 16) * 8 + c row-wise and
+//     c * 8 + r / 16 column-wise (the same table: tile (ty, tx) at ty * 8 + tx).
+constexpr int kScPitchRow = 160, kScPitchCol = 192;
+constexpr int kScRegion = 8 * kScPitchCol;  // bytes per direction
+
+template <int MODE, bool kColDir>
+__device__ __forceinline__ uint32_t staged_scale(const uint8_t* s, int r, int c) {
+  if constexpr (MODE == kCast2D)
+    return kColDir ? s[c * 8 + (r >> 4)] : s[(r >> 4) * 8 + c];
+  else
+    return s[c * (kColDir ? kScPitchCol : kScPitchRow) + r];
+}
+
+// stages | 2 encode-factor tables | 2 x 2 staged scale regions | barriers | flag
 template <typename T>
 __host__ __device__ constexpr size_t smem_bytes() {
-  return 1024 + (size_t)TileCfg<T>::kStages * tile_bytes<T>() + 2 * 128 * 4 + 4 * 1024 +
+  return 1024 + (size_t)TileCfg<T>::kStages * tile_bytes<T>() + 2 * 128 * 4 + 4 * kScRegion +
          8 * TileCfg<T>::kStages + 16;
 }
 
@@ -249,8 +268,8 @@ __device__ __forceinline__ float tile_max(const Sub<T>& s) {
 
 // Casts this thread's 8x8 sub-block of the staged tile at shared address
 // `stage`: stores its code words and stages its scales in the shared
-// buffers at sc_row ([128][8], by tile row) and sc_col ([128][8], by tile
-// column).  `warp` is the warp's index within the 8 warps casting the tile.
+// regions at sc_row and sc_col (layouts: staged_scale).  `warp` is the
+// warp's index within the 8 warps casting the tile.
 // kDirs: 3 = both directions, 1 = row-wise only, 2 = column-wise only.
 // kInterior: the whole 128x128 tile lies inside x (no bounds checks).
 template <typename T, int MODE, int kDirs, bool kInterior>
@@ -294,8 +313,9 @@ __device__ __forceinline__ void block_pass(uint32_t stage, const float* rtab_row
       st_cs_u32_if(pcol, w, (col_ok >> c) & 1u);
     pcol += scol;
   };
-  const uint32_t srow_st = sc_row + trow * 8 + (tcol >> 4);  // staged row scales, one byte per row
-  const uint32_t scol_st = sc_col + tcol * 8 + (trow >> 4);  // staged column scales, one per column
+  // The first of the two lanes of a 1x16 row block (j even) stages its rows'
+  // scales, the first of the two of a 16x1 column block (i even) its
+  // columns' scales; in 2D the first of the four lanes of a 16x16 tile.
   const bool stage_row = (j & 1) == 0, stage_col = (i & 1) == 0;
 
   if constexpr (MODE == kCast2D) {
@@ -315,17 +335,15 @@ __device__ __forceinline__ void block_pass(uint32_t stage, const float* rtab_row
 #pragma unroll
       for (int c = 0; c < 8; ++c) put_col(c, wc[c]);
     }
-    if (kRow && stage_row) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sts_u8(srow_st + 8 * k, sr);
-    }
-    if (kCol && stage_col) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) sts_u8(scol_st + 8 * c, sc);
+    if (stage_row && stage_col) {
+      const uint32_t o = (uint32_t)((trow >> 4) * 8 + (tcol >> 4));
+      if (kRow) sts_u8(sc_row + o, sr);
+      if (kCol) sts_u8(sc_col + o, sc);
     }
   } else {
     // 1D: row blocks 1x16 (lanes l, l^1), column blocks 16x1 (lanes l, l^8).
     if (kRow) {
+      uint32_t packed[2] = {0u, 0u};  // byte k: scale of row trow + k
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         float m0, m1;
@@ -340,13 +358,12 @@ __device__ __forceinline__ void block_pass(uint32_t stage, const float* rtab_row
         const uint32_t s0 = block_scale(m0, g_row), s1 = block_scale(m1, g_row);
         put_row(2 * t, encode_row<T>(s, 2 * t, rtab_row[s0]));
         put_row(2 * t + 1, encode_row<T>(s, 2 * t + 1, rtab_row[s1]));
-        if (stage_row) {
-          sts_u8(srow_st + 16 * t, s0);
-          sts_u8(srow_st + 16 * t + 8, s1);
-        }
+        packed[t >> 1] |= (s0 | (s1 << 8)) << (16 * (t & 1));
       }
+      if (stage_row) sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
     }
     if (kCol) {
+      uint32_t packed[2] = {0u, 0u};  // byte c: scale of column tcol + c
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         float m0, m1;
@@ -361,11 +378,9 @@ __device__ __forceinline__ void block_pass(uint32_t stage, const float* rtab_row
         const uint32_t s0 = block_scale(m0, g_col), s1 = block_scale(m1, g_col);
         put_col(2 * p, encode_col<T>(s, 2 * p, rtab_col[s0]));
         put_col(2 * p + 1, encode_col<T>(s, 2 * p + 1, rtab_col[s1]));
-        if (stage_col) {
-          sts_u8(scol_st + 16 * p, s0);
-          sts_u8(scol_st + 16 * p + 8, s1);
-        }
+        packed[p >> 1] |= (s0 | (s1 << 8)) << (16 * (p & 1));
       }
+      if (stage_col) sts_v2(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), packed[0], packed[1]);
     }
   }
 }
@@ -395,8 +410,10 @@ __device__ __forceinline__ void block_pass_any(uint32_t stage, const float* rtab
   }
 }
 
-// Stores one direction's staged scale tile [128 rows][8 scale columns] at
-// rows R0.., scale columns C0.. of an R x C scale matrix; t = 0..127.
+// Stores one direction's staged scales (layout: staged_scale<MODE, kColDir>)
+// for tile rows R0 .. R0 + 127 and scale columns C0 .. C0 + 7 of an R x C
+// scale matrix; t = 0..127.
+template <int MODE, bool kColDir>
 __device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out, int64_t R0, int64_t C0, int64_t R,
                                                  int64_t C, bool swizzled, int t) {
   if (swizzled) {
@@ -406,7 +423,16 @@ __device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out,
     const int h = t >> 5, L = t & 31;
     uint32_t w[4];
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) w[qq] = *reinterpret_cast<const uint32_t*>(s + (32 * qq + L) * 8 + 4 * h);
+    for (int qq = 0; qq < 4; ++qq) {
+      const int r = 32 * qq + L;
+      if constexpr (MODE == kCast2D && !kColDir) {
+        w[qq] = *reinterpret_cast<const uint32_t*>(s + (r >> 4) * 8 + 4 * h);
+      } else {
+        w[qq] = staged_scale<MODE, kColDir>(s, r, 4 * h) | (staged_scale<MODE, kColDir>(s, r, 4 * h + 1) << 8) |
+                (staged_scale<MODE, kColDir>(s, r, 4 * h + 2) << 16) |
+                (staged_scale<MODE, kColDir>(s, r, 4 * h + 3) << 24);
+      }
+    }
     uint8_t* base = out + ((R0 >> 7) * (C >> 2) + (C0 >> 2) + h) * 512 + L * 16;
     st_cs_v4(base, w[0], w[1], w[2], w[3]);
   } else {
@@ -415,11 +441,22 @@ __device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out,
     const int64_t n = (C - C0) < 8 ? (C - C0) : 8;
     if (n <= 0) return;
     uint8_t* p = out + r * C + C0;
-    const uint2 v = *reinterpret_cast<const uint2*>(s + t * 8);
-    if (n == 8 && (reinterpret_cast<uintptr_t>(p) & 7) == 0) {
-      st_cs_v2(p, v.x, v.y);
+    uint32_t v[2];
+    if constexpr (MODE == kCast2D && !kColDir) {
+      const uint2 u = *reinterpret_cast<const uint2*>(s + (t >> 4) * 8);
+      v[0] = u.x;
+      v[1] = u.y;
     } else {
-      for (int b = 0; b < n; ++b) st_cs_u8(p + b, (b < 4 ? v.x : v.y) >> (8 * (b & 3)));
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        v[hh] = staged_scale<MODE, kColDir>(s, t, 4 * hh) | (staged_scale<MODE, kColDir>(s, t, 4 * hh + 1) << 8) |
+                (staged_scale<MODE, kColDir>(s, t, 4 * hh + 2) << 16) |
+                (staged_scale<MODE, kColDir>(s, t, 4 * hh + 3) << 24);
+    }
+    if (n == 8 && (reinterpret_cast<uintptr_t>(p) & 7) == 0) {
+      st_cs_v2(p, v[0], v[1]);
+    } else {
+      for (int b = 0; b < n; ++b) st_cs_u8(p + b, v[b >> 2] >> (8 * (b & 3)));
     }
   }
 }
