@@ -233,6 +233,14 @@ __device__ __forceinline__ void sts_u8(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void sts_v2(uint32_t addr, uint32_t a, uint32_t b) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void st_cs_v2_if(void* p, uint32_t a, uint32_t b, bool pred) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %3, 0;\n @q st.global.cs.v2.u32 [%0], {%1, %2};\n}" ::"l"(p),
+               "r"(a), "r"(b), "r"((uint32_t)pred)
+               : "memory");
+}
 __device__ __forceinline__ void st_cs_u16(void* p, uint32_t a) {
   asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(a)) : "memory");
 }

@@ -1,15 +1,19 @@
 // fused.cu -- single-launch NVFP4 quantize: per-tensor amax and the fused
 // row-wise + column-wise cast in one persistent kernel.
 //
-// One CTA per SM (cooperative launch, all CTAs co-resident), 16 warps in two
-// groups of 8; a group casts one 128x128 tile at a time:
-//   * a stage's TMA completion is an mbarrier; when the 8 warps of a group
-//     are done with a stage, the last of them (a shared-memory counter per
-//     stage) writes the tile's staged scales back and issues the next load
-//     into the stage, so no warp ever waits for the whole CTA;
-//   * phase A streams the CTA's tiles t_k = blockIdx + k * gridDim through
-//     the stage ring computing max|x|; the last kStages tiles stay in shared
-//     memory;
+// One CTA per SM (cooperative launch, all CTAs co-resident), 16 warps in
+// groups; a group casts one 128x128 tile at a time (BF16: groups of 4 warps
+// with the wide 8x16-per-lane mapping, FP32: groups of 8 with 8x8 sub-blocks):
+//   * tile k of the CTA (t_k = blockIdx + k * gridDim) goes through stage
+//     k % S of a shared-memory ring and is handled by group k % groups; its
+//     TMA completion is an mbarrier whose phase parity is (k / S) & 1 in both
+//     phases (the fills of a stage are sequential);
+//   * when the warps of a group are done with a stage, the last of them (a
+//     shared-memory counter per stage) writes the tile's staged scales back
+//     and issues the next load into the stage, so no warp ever waits for the
+//     whole CTA;
+//   * phase A streams the CTA's tiles through the ring computing max|x|; the
+//     last S tiles stay in shared memory;
 //   * a grid barrier in the caller's workspace combines the CTA maxima
 //     (the amax is written to both direction buffers, "Write both NVFP4 amax
 //     buffers");
@@ -29,25 +33,26 @@ namespace {
 
 using namespace tile;
 
-constexpr int kGroups = 2;                       // warp groups
-constexpr int kWarps = 8 * kGroups;              // 8 warps cast one tile
+constexpr int kWarps = 16;
 constexpr int kFusedThreads = 32 * kWarps;
 
 template <typename T>
 struct FusedCfg;
 template <>
 struct FusedCfg<uint16_t> {
-  static constexpr int kStages = 6;  // even: stage parity = consumer group
+  static constexpr int kStages = 6;
+  static constexpr int kWarpsPerTile = 4;  // wide mapping
 };
 template <>
 struct FusedCfg<float> {
   static constexpr int kStages = 2;
+  static constexpr int kWarpsPerTile = 8;  // 8x8 sub-blocks
 };
 
 template <typename T>
 __host__ __device__ constexpr size_t fused_smem_bytes() {
   return 1024 + (size_t)FusedCfg<T>::kStages * (tile_bytes<T>() + 2 * kScRegion) + 2 * 128 * 4 +
-         16 * FusedCfg<T>::kStages + 64 * 4 + 64;
+         20 * FusedCfg<T>::kStages + 64 * 4 + 64;
 }
 
 struct FSmem {
@@ -58,6 +63,7 @@ struct FSmem {
   uint64_t* full;    // [S]
   unsigned* done;    // [S] warps of the current group done with the stage
   unsigned* issued;  // [S] loads issued into the stage so far
+  int* tile_in;      // [S] tile index of the stage's latest issued load
   float* red;        // [64]
   float* amax;       // [1] broadcast of the global amax
   int* abort_flag;   // [1]
@@ -79,7 +85,8 @@ __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
   s.full = reinterpret_cast<uint64_t*>(s.rtab_col + 128);
   s.done = reinterpret_cast<unsigned*>(s.full + S);
   s.issued = s.done + S;
-  s.red = reinterpret_cast<float*>(s.issued + S);
+  s.tile_in = reinterpret_cast<int*>(s.issued + S);
+  s.red = reinterpret_cast<float*>(s.tile_in + S);
   s.amax = s.red + 64;
   s.abort_flag = reinterpret_cast<int*>(s.amax + 1);
   return s;
@@ -145,21 +152,26 @@ __device__ bool grid_max(SinglePassWorkspace* ws, float m, unsigned n_cta, unsig
   return true;
 }
 
-// max|x| over this thread's 8x8 sub-block of a staged tile (as a packed pair
-// for BF16, a float for FP32).
+// max|x| over this warp's share of a staged tile: BF16, a quarter of the
+// tile (8 KB, sixteen 16-byte loads per lane, consecutive lanes on
+// consecutive chunks); FP32, its 8x8 sub-block.
 template <typename T>
-__device__ __forceinline__ float sub_absmax(uint32_t stage, int cw) {
+__device__ __forceinline__ float share_absmax(uint32_t stage, int cw) {
   const int lane = threadIdx.x & 31;
-  const int bx = cw & 1, q = cw >> 1, j = lane & 7, i = lane >> 3;
-  Sub<T> s;
-  load_sub<T>(stage, bx, 32 * q + 8 * i, j, s);
   if constexpr (sizeof(T) == 2) {
+    const uint32_t base = stage + (uint32_t)cw * 8192u + (uint32_t)lane * 16u;
     uint32_t acc = 0;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc = xsa(acc, xsa(xsa(s.w[k][0], s.w[k][1]), xsa(s.w[k][2], s.w[k][3])));
+    for (int k = 0; k < 16; ++k) {
+      const uint4 v = lds128(base + 512u * k);
+      acc = xsa(acc, xsa(xsa(v.x, v.y), xsa(v.z, v.w)));
+    }
     acc &= 0x7FFF7FFFu;
     return fmaxf(bf16_lo(acc), bf16_hi(acc));
   } else {
+    const int bx = cw & 1, q = cw >> 1, j = lane & 7, i = lane >> 3;
+    Sub<T> s;
+    load_sub<T>(stage, bx, 32 * q + 8 * i, j, s);
     float m = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -173,6 +185,8 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tmap, const CastArgs a, SinglePassWorkspace* ws) {
   constexpr int S = FusedCfg<T>::kStages;
+  constexpr int WPT = FusedCfg<T>::kWarpsPerTile;
+  constexpr int kGroups = kWarps / WPT;
   extern __shared__ uint8_t smem_raw[];
   const FSmem sm = fcarve<T>(smem_raw);
   if (a.noop != nullptr && *a.noop == 1.0f) return;
@@ -197,6 +211,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     tile_rc(k, r0, c0);
     uint8_t* dst = sm.stages + (size_t)s * tile_bytes<T>();
     sm.issued[s] += 1;
+    *reinterpret_cast<volatile int*>(&sm.tile_in[s]) = k;  // before the arrival (see wait_full)
     mbar_arrive_expect_tx(&sm.full[s], tile_bytes<T>());
 #pragma unroll
     for (int bb = 0; bb < TileCfg<T>::kBoxes; ++bb)
@@ -208,6 +223,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       mbar_init(&sm.full[s], 1);
       sm.done[s] = 0;
       sm.issued[s] = 0;
+      sm.tile_in[s] = -1;
     }
     *sm.abort_flag = 0;
     fence_mbar_init();
@@ -216,8 +232,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   __syncthreads();
 
-  // A warp done with stage s counts itself; the 8th (last) warp of the group
-  // may then reuse the stage: it runs `refill` with all 32 lanes.  The fences
+  // A warp done with stage s counts itself; the last warp of the group may
+  // then reuse the stage: it runs `refill` with all 32 lanes.  The fences
   // make the other warps' shared-memory reads and staged scales happen
   // before the refill.
   auto finish_stage = [&](int s, auto&& refill) {
@@ -225,7 +241,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     unsigned last = 0;
     if (lane == 0) {
       __threadfence_block();
-      last = (atomicAdd(&sm.done[s], 1u) == 7u) ? 1u : 0u;
+      last = (atomicAdd(&sm.done[s], 1u) == (unsigned)(WPT - 1)) ? 1u : 0u;
       if (last) {
         sm.done[s] = 0;
         __threadfence_block();
@@ -237,25 +253,47 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   };
 
-  const int grp = warp >> 3, cw = warp & 7;
-  unsigned full_par = 0;  // bit s: parity of the next load of stage s (this group's stages)
+  const int grp = warp / WPT, cw = warp % WPT;
   bool ok = true;
-  auto wait_full = [&](int s) {
-    const bool w = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.full[s], (full_par >> s) & 1u, a.status));
-    full_par ^= 1u << s;
-    return w;
+  // Waits until tile k is in its stage.  The stage's previous tile belongs
+  // to another group, which may not be done with it yet: a parity wait
+  // issued before tile k's load would refer to that earlier phase.  So lane
+  // 0 first waits (bounded) until tile k's load has been issued (tile_in[s]
+  // is set before its arrival), which also means the earlier phase is
+  // complete.  Tile k's load is the stage's fill number k / S in phase A;
+  // in phase B a stage's tiles are reloaded in reverse order after its F
+  // phase-A fills, tile s + m S as fill 2F - 2 - m: the parity is (k / S) & 1
+  // in both phases.
+  auto wait_full = [&](int k) {
+    const int s = k % S;
+    unsigned issued_ok = 1;
+    if (lane == 0) {
+      const volatile int* slot = &sm.tile_in[s];
+      if (*slot != k) {
+        const long long t0 = clock64();
+        while (*slot != k) {
+          if (clock64() - t0 > kWaitLimitCycles) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            issued_ok = 0;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+    }
+    if (!__shfl_sync(0xFFFFFFFFu, issued_ok, 0)) return false;
+    return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.full[s], (uint32_t)((k / S) & 1), a.status)) != 0;
   };
 
-  // phase A: max|x| of this group's tiles (k == grp mod 2; stage k % S has
-  // the same parity because S is even)
+  // phase A: max|x| of this group's tiles (k == grp mod kGroups)
   float m = 0.0f;
   for (int k = grp; k < n; k += kGroups) {
     const int s = k % S;
-    if (!wait_full(s)) {
+    if (!wait_full(k)) {
       ok = false;
       break;
     }
-    m = fmaxf(m, sub_absmax<T>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), cw));
+    m = fmaxf(m, share_absmax<T>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), cw));
     if (k + S < n) {  // tile k leaves shared memory: load tile k + S into its stage
       finish_stage(s, [&] {
         if (lane == 0) issue(k + S, k + S >= kept_from ? stream : keep);
@@ -303,15 +341,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // phase B: descending k, this group's tiles; the last warp done with a
   // tile writes its scales back and reloads tile k - S into the stage
   const bool do_row = a.rowwise != 0, do_col = a.colwise != 0;
-  const int k_top = ((n - 1) & 1) == grp ? n - 1 : n - 2;
+  const int k_top = n - 1 - ((n - 1 - grp) % kGroups + kGroups) % kGroups;  // largest k < n, k == grp mod kGroups
   for (int k = k_top; k >= 0; k -= kGroups) {
     const int s = k % S;
-    if (k < kept_from && !wait_full(s)) return;  // the waiting CTA gives up; outputs unfinished
+    if (k < kept_from && !wait_full(k)) return;  // the waiting CTA gives up; outputs unfinished
     int64_t r0, c0;
     tile_rc(k, r0, c0);
     uint8_t* sc = sm.sc + (size_t)s * 2 * kScRegion;
-    block_pass_any<T, MODE>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), sm.rtab_row, sm.rtab_col,
-                            smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, g, do_row, do_col, cw);
+    const uint32_t st = smem_u32(sm.stages + (size_t)s * tile_bytes<T>());
+    if constexpr (sizeof(T) == 2)
+      wide_pass_any<MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, g,
+                          do_row, do_col, cw);
+    else
+      block_pass_any<T, MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g,
+                              g, do_row, do_col, cw);
     finish_stage(s, [&] {
       for (int t = lane; t < 128; t += 32) {
         if (do_row) store_scale_tile<MODE, false>(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);

@@ -410,6 +410,217 @@ __device__ __forceinline__ void block_pass_any(uint32_t stage, const float* rtab
   }
 }
 
+// ---------------------------------------------------------------------------
+// Wide sub-tiles (BF16): four warps cast a 128x128 tile, warp w owning the
+// 64x64 quarter at rows 64 (w >> 1), columns 64 (w & 1) (box w & 1); lane l
+// owns 8 rows x 16 columns: rows 64 (w >> 1) + 8 i, columns 64 (w & 1) + 16 j,
+// i = l >> 2, j = l & 3.  Every code store of a warp then fills whole 32-byte
+// sectors: a row-wise store writes 16 columns (8 bytes) per lane and the four
+// lanes of a row are adjacent; a column-wise store writes 8 rows (4 bytes)
+// per lane and the eight lanes of a column are adjacent.  A 1x16 row block
+// lies inside one lane; a 16x1 column block and a 16x16 tile span lanes l
+// and l ^ 4.
+//
+// The 16 columns are two 16-byte chunks (2j and 2j + 1 of the 128-byte row
+// of box w & 1).  Lanes with odd i load them in the other order ("A" is
+// chunk 2j + (i & 1), "B" the other one), so that each quarter-warp of a
+// 16-byte shared load touches eight different chunks (no bank conflicts).
+// ---------------------------------------------------------------------------
+struct SubW {
+  uint32_t a[8][4], b[8][4];  // [row k][BF16 pair]: halves A and B
+};
+
+__device__ __forceinline__ void load_sub_w(uint32_t stage, int wc, int trow, int j, int par, SubW& s) {
+  const uint32_t base = stage + wc * kBoxBytes + trow * 128;
+  const uint32_t ca = (uint32_t)(2 * j + par) << 4, cb = ca ^ 16u;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 va = lds128(base + 128 * k + (ca ^ (k << 4)));
+    const uint4 vb = lds128(base + 128 * k + (cb ^ (k << 4)));
+    s.a[k][0] = va.x; s.a[k][1] = va.y; s.a[k][2] = va.z; s.a[k][3] = va.w;
+    s.b[k][0] = vb.x; s.b[k][1] = vb.y; s.b[k][2] = vb.z; s.b[k][3] = vb.w;
+  }
+}
+
+// Codes of row k of one half (8 values), v0 in the low nibble.
+__device__ __forceinline__ uint32_t encode_half_row(const uint32_t (&w)[4], float r) {
+  return encode8(bf16_lo(w[0]), bf16_hi(w[0]), bf16_lo(w[1]), bf16_hi(w[1]), bf16_lo(w[2]), bf16_hi(w[2]),
+                 bf16_lo(w[3]), bf16_hi(w[3]), r);
+}
+// Codes of column c (0..7) of one half over the 8 rows, row 0 in the low nibble.
+__device__ __forceinline__ uint32_t encode_half_col(const uint32_t (&w)[8][4], int c, float r) {
+  const int p = c >> 1;
+  if (c & 1)
+    return encode8(bf16_hi(w[0][p]), bf16_hi(w[1][p]), bf16_hi(w[2][p]), bf16_hi(w[3][p]), bf16_hi(w[4][p]),
+                   bf16_hi(w[5][p]), bf16_hi(w[6][p]), bf16_hi(w[7][p]), r);
+  return encode8(bf16_lo(w[0][p]), bf16_lo(w[1][p]), bf16_lo(w[2][p]), bf16_lo(w[3][p]), bf16_lo(w[4][p]),
+                 bf16_lo(w[5][p]), bf16_lo(w[6][p]), bf16_lo(w[7][p]), r);
+}
+// Packed (max|.| of row k0, of row k1) over both halves (16 columns).
+__device__ __forceinline__ uint32_t row_pair_max_w(const SubW& s, int k0, int k1) {
+  const uint32_t x = xsa(xsa(xsa(s.a[k0][0], s.a[k0][1]), xsa(s.a[k0][2], s.a[k0][3])),
+                         xsa(xsa(s.b[k0][0], s.b[k0][1]), xsa(s.b[k0][2], s.b[k0][3])));
+  const uint32_t y = xsa(xsa(xsa(s.a[k1][0], s.a[k1][1]), xsa(s.a[k1][2], s.a[k1][3])),
+                         xsa(xsa(s.b[k1][0], s.b[k1][1]), xsa(s.b[k1][2], s.b[k1][3])));
+  return xsa_pairs(x, y) & 0x7FFF7FFFu;
+}
+// Packed (max|.| of column 2p, of column 2p+1) of one half over its 8 rows.
+__device__ __forceinline__ uint32_t col_pair_acc_w(const uint32_t (&w)[8][4], int p) {
+  return xsa(xsa(xsa(w[0][p], w[1][p]), xsa(w[2][p], w[3][p])), xsa(xsa(w[4][p], w[5][p]), xsa(w[6][p], w[7][p])));
+}
+
+// Casts this lane's 8x16 sub-tile (wide mapping) of the staged tile at shared
+// address `stage`: stores its codes and stages its scales (staged_scale
+// layouts) at sc_row / sc_col.  `warp` is the warp's index (0..3) among the
+// four casting the tile.  kDirs: 3 both directions, 1 row-wise, 2
+// column-wise.  kInterior: the tile lies inside x.
+template <int MODE, int kDirs, bool kInterior>
+__device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row, const float* rtab_col,
+                                          uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
+                                          int64_t c0, float g_row, float g_col, int warp) {
+  constexpr bool kRow = (kDirs & 1) != 0, kCol = (kDirs & 2) != 0;
+  const int lane = threadIdx.x & 31;
+  const int wr = warp >> 1, wc = warp & 1, i = lane >> 2, j = lane & 3, par = i & 1;
+  const int trow = 64 * wr + 8 * i, tcol = 64 * wc + 16 * j;
+  SubW s;
+  load_sub_w(stage, wc, trow, j, par, s);
+
+  const int64_t M = a.M, N = a.N, y0 = r0 + trow, x0 = c0 + tcol;
+  const int64_t srow = N / 2, scol = M / 2;
+  uint8_t* prow = kRow ? a.data_row + y0 * srow + x0 / 2 : nullptr;
+  uint8_t* pcol = kCol ? a.data_col + x0 * scol + y0 / 2 : nullptr;
+  // Outside x (edge tiles only): N % 16 == 0, so the 16 columns are all in
+  // or all out; column-wise output needs M % 16 == 0, so then the 8 rows
+  // are too; row-wise alone allows any M (per-row predicates).
+  const bool cols_in = kInterior || x0 < N;
+  const bool rows_in = kInterior || y0 < M;
+  auto put_row = [&](int k, uint32_t wa, uint32_t wb) {
+    const uint32_t lo = par ? wb : wa, hi = par ? wa : wb;
+    if (kInterior)
+      st_cs_v2(prow + k * srow, lo, hi);
+    else
+      st_cs_v2_if(prow + k * srow, lo, hi, cols_in && y0 + k < M);
+  };
+  // column cc (0..15) of the lane's 16; half A holds columns 8 par .. 8 par + 7
+  auto put_col = [&](int cc, uint32_t w) {
+    if (kInterior)
+      st_cs_u32(pcol + cc * scol, w);
+    else
+      st_cs_u32_if(pcol + cc * scol, w, (cols_in && rows_in) ? 1u : 0u);
+  };
+
+  if constexpr (MODE == kCast2D) {
+    // 16x16 tile: this lane's 128 values and lane l ^ 4's
+    uint32_t acc = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      acc = xsa(acc, xsa(xsa(xsa(s.a[k][0], s.a[k][1]), xsa(s.a[k][2], s.a[k][3])),
+                         xsa(xsa(s.b[k][0], s.b[k][1]), xsa(s.b[k][2], s.b[k][3]))));
+    acc &= 0x7FFF7FFFu;
+    float m = fmaxf(bf16_lo(acc), bf16_hi(acc));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    const uint32_t sr = block_scale(m, g_row);
+    const uint32_t sc = (g_col == g_row) ? sr : block_scale(m, g_col);
+    const float rr = rtab_row[sr], rc = rtab_col[sc];
+    uint32_t ca[8], cb[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t wa = encode_half_row(s.a[k], kRow ? rr : rc);
+      const uint32_t wb = encode_half_row(s.b[k], kRow ? rr : rc);
+      if (kRow) put_row(k, wa, wb);
+      if (kCol) {
+        const bool same = !kRow || rc == rr;
+        ca[k] = same ? wa : encode_half_row(s.a[k], rc);
+        cb[k] = same ? wb : encode_half_row(s.b[k], rc);
+      }
+    }
+    if (kCol) {
+      transpose_nibbles8x8(ca);
+      transpose_nibbles8x8(cb);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        put_col(c, par ? cb[c] : ca[c]);
+        put_col(8 + c, par ? ca[c] : cb[c]);
+      }
+    }
+    if (par == 0) {
+      const uint32_t o = (uint32_t)((trow >> 4) * 8 + (tcol >> 4));
+      if (kRow) sts_u8(sc_row + o, sr);
+      if (kCol) sts_u8(sc_col + o, sc);
+    }
+  } else {
+    // column pass first, then the row pass: only the data stay live between them
+    if (kCol) {
+      // column blocks span lanes l and l ^ 4, whose halves A are the other
+      // side of the 16 columns: combine left with left, right with right
+      uint32_t pl[2] = {0u, 0u}, pr[2] = {0u, 0u};  // byte c: scale of left / right column c
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t xa = col_pair_acc_w(s.a, p), xb = col_pair_acc_w(s.b, p);
+        uint32_t ml = par ? xb : xa, mr = par ? xa : xb;
+        ml = xsa(ml, __shfl_xor_sync(0xFFFFFFFFu, ml, 4)) & 0x7FFF7FFFu;
+        mr = xsa(mr, __shfl_xor_sync(0xFFFFFFFFu, mr, 4)) & 0x7FFF7FFFu;
+        const uint32_t sl0 = block_scale(bf16_lo(ml), g_col), sl1 = block_scale(bf16_hi(ml), g_col);
+        const uint32_t sr0 = block_scale(bf16_lo(mr), g_col), sr1 = block_scale(bf16_hi(mr), g_col);
+        const float fl0 = rtab_col[sl0], fl1 = rtab_col[sl1], fr0 = rtab_col[sr0], fr1 = rtab_col[sr1];
+        const uint32_t wa0 = encode_half_col(s.a, 2 * p, par ? fr0 : fl0);
+        const uint32_t wa1 = encode_half_col(s.a, 2 * p + 1, par ? fr1 : fl1);
+        const uint32_t wb0 = encode_half_col(s.b, 2 * p, par ? fl0 : fr0);
+        const uint32_t wb1 = encode_half_col(s.b, 2 * p + 1, par ? fl1 : fr1);
+        put_col(2 * p, par ? wb0 : wa0);
+        put_col(2 * p + 1, par ? wb1 : wa1);
+        put_col(8 + 2 * p, par ? wa0 : wb0);
+        put_col(8 + 2 * p + 1, par ? wa1 : wb1);
+        pl[p >> 1] |= (sl0 | (sl1 << 8)) << (16 * (p & 1));
+        pr[p >> 1] |= (sr0 | (sr1 << 8)) << (16 * (p & 1));
+      }
+      if (par == 0)  // lanes l and l ^ 4 hold the same column-block scales
+        sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), pl[0], pl[1], pr[0], pr[1]);
+    }
+    if (kRow) {
+      // with both directions, re-read the sub-tile (still staged): keeping
+      // its 64 data registers live through the column pass exceeds the
+      // register budget
+      if (kCol) load_sub_w(stage, wc, trow, j, par, s);
+      uint32_t packed[2] = {0u, 0u};  // byte k: scale of row trow + k
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t pr = row_pair_max_w(s, 2 * t, 2 * t + 1);
+        const uint32_t s0 = block_scale(bf16_lo(pr), g_row), s1 = block_scale(bf16_hi(pr), g_row);
+        const float f0 = rtab_row[s0], f1 = rtab_row[s1];
+        put_row(2 * t, encode_half_row(s.a[2 * t], f0), encode_half_row(s.b[2 * t], f0));
+        put_row(2 * t + 1, encode_half_row(s.a[2 * t + 1], f1), encode_half_row(s.b[2 * t + 1], f1));
+        packed[t >> 1] |= (s0 | (s1 << 8)) << (16 * (t & 1));
+      }
+      sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void wide_pass_any(uint32_t stage, const float* rtab_row, const float* rtab_col,
+                                              uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
+                                              int64_t c0, float g_row, float g_col, bool do_row, bool do_col,
+                                              int warp) {
+  const bool interior = (r0 + kTile <= a.M) && (c0 + kTile <= a.N);
+  if (do_row && do_col) {
+    if (interior)
+      wide_pass<MODE, 3, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+    else
+      wide_pass<MODE, 3, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+  } else if (do_row) {
+    if (interior)
+      wide_pass<MODE, 1, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+    else
+      wide_pass<MODE, 1, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+  } else if (do_col) {
+    if (interior)
+      wide_pass<MODE, 2, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+    else
+      wide_pass<MODE, 2, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+  }
+}
+
 // Stores one direction's staged scales (layout: staged_scale<MODE, kColDir>)
 // for tile rows R0 .. R0 + 127 and scale columns C0 .. C0 + 7 of an R x C
 // scale matrix; t = 0..127.
