@@ -52,7 +52,7 @@ struct FusedCfg<float> {
 template <typename T>
 __host__ __device__ constexpr size_t fused_smem_bytes() {
   return 1024 + (size_t)FusedCfg<T>::kStages * (tile_bytes<T>() + 2 * kScRegion) + 2 * 128 * 4 +
-         20 * FusedCfg<T>::kStages + 64 * 4 + 64;
+         28 * FusedCfg<T>::kStages + 16 + 64 * 4 + 64;
 }
 
 struct FSmem {
@@ -61,13 +61,29 @@ struct FSmem {
   float* rtab_row;   // [128]
   float* rtab_col;   // [128]
   uint64_t* full;    // [S]
-  unsigned* done;    // [S] warps of the current group done with the stage
+  unsigned* done;    // [S] warps done with the staged scales of the stage's tile
+  unsigned* loaded;  // [S] warps done reading the stage's tile data
   unsigned* issued;  // [S] loads issued into the stage so far
   int* tile_in;      // [S] tile index of the stage's latest issued load
+  int* sc_owner;     // [S] tile allowed to write the stage's scale region
+  unsigned* exited;  // [1] warps done with phase B
   float* red;        // [64]
   float* amax;       // [1] broadcast of the global amax
   int* abort_flag;   // [1]
 };
+
+// The two stage hooks the cast passes call (see wide_pass).
+template <class D, class W>
+struct StageHooksT {
+  D done_fn;
+  W wait_fn;
+  __device__ __forceinline__ void data_done(uint32_t token) const { done_fn(token); }
+  __device__ __forceinline__ void scale_wait() const { wait_fn(); }
+};
+template <class D, class W>
+__device__ __forceinline__ StageHooksT<D, W> make_hooks(D d, W w) {
+  return StageHooksT<D, W>{d, w};
+}
 
 template <typename T>
 __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
@@ -84,9 +100,12 @@ __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
   s.rtab_col = s.rtab_row + 128;
   s.full = reinterpret_cast<uint64_t*>(s.rtab_col + 128);
   s.done = reinterpret_cast<unsigned*>(s.full + S);
-  s.issued = s.done + S;
+  s.loaded = s.done + S;
+  s.issued = s.loaded + S;
   s.tile_in = reinterpret_cast<int*>(s.issued + S);
-  s.red = reinterpret_cast<float*>(s.tile_in + S);
+  s.sc_owner = s.tile_in + S;
+  s.exited = reinterpret_cast<unsigned*>(s.sc_owner + S);
+  s.red = reinterpret_cast<float*>(s.exited + 4);
   s.amax = s.red + 64;
   s.abort_flag = reinterpret_cast<int*>(s.amax + 1);
   return s;
@@ -222,35 +241,54 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&sm.full[s], 1);
       sm.done[s] = 0;
+      sm.loaded[s] = 0;
       sm.issued[s] = 0;
       sm.tile_in[s] = -1;
+      sm.sc_owner[s] = -1;
     }
     *sm.abort_flag = 0;
+    *sm.exited = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap);
     for (int k = 0; k < S && k < n; ++k) issue(k, k >= kept_from ? stream : keep);
   }
   __syncthreads();
 
-  // A warp done with stage s counts itself; the last warp of the group may
-  // then reuse the stage: it runs `refill` with all 32 lanes.  The fences
-  // make the other warps' shared-memory reads and staged scales happen
-  // before the refill.
-  auto finish_stage = [&](int s, auto&& refill) {
-    __syncwarp();
-    unsigned last = 0;
+  // A warp done reading stage s's tile data counts itself; the last of the
+  // group's warps loads tile `next` (if any) into the stage.  The count's
+  // address depends on `token`, a value computed from every word the warp
+  // read (warp-wide registers), so the count cannot be performed before
+  // those reads have completed.
+  auto release_data = [&](int s, int next, uint64_t pol, uint32_t token) {
     if (lane == 0) {
-      __threadfence_block();
-      last = (atomicAdd(&sm.done[s], 1u) == (unsigned)(WPT - 1)) ? 1u : 0u;
-      if (last) {
-        sm.done[s] = 0;
+      uint32_t zero;
+      asm volatile("and.b32 %0, %1, 0;" : "=r"(zero) : "r"(token));
+      if (atomicAdd(&sm.loaded[s] + zero, 1u) == (unsigned)(WPT - 1)) {
+        sm.loaded[s] = 0;
         __threadfence_block();
+        if (next >= 0) issue(next, pol);
       }
     }
-    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-      __syncwarp();  // the lanes' reads below come after lane 0's acquire
-      refill();
+  };
+  // Bounded wait of lane 0 until *slot == want (a shared-memory hand-over
+  // between warps); false when it ran out.
+  auto wait_slot = [&](const int* p, int want) {
+    unsigned good = 1;
+    if (lane == 0) {
+      const volatile int* slot = p;
+      if (*slot != want) {
+        const long long t0 = clock64();
+        while (*slot != want) {
+          if (clock64() - t0 > kWaitLimitCycles) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            good = 0;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
     }
+    return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
   };
 
   const int grp = warp / WPT, cw = warp % WPT;
@@ -266,22 +304,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // in both phases.
   auto wait_full = [&](int k) {
     const int s = k % S;
-    unsigned issued_ok = 1;
-    if (lane == 0) {
-      const volatile int* slot = &sm.tile_in[s];
-      if (*slot != k) {
-        const long long t0 = clock64();
-        while (*slot != k) {
-          if (clock64() - t0 > kWaitLimitCycles) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            issued_ok = 0;
-            break;
-          }
-          __nanosleep(64);
-        }
-      }
-    }
-    if (!__shfl_sync(0xFFFFFFFFu, issued_ok, 0)) return false;
+    if (!wait_slot(&sm.tile_in[s], k)) return false;
     return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.full[s], (uint32_t)((k / S) & 1), a.status)) != 0;
   };
 
@@ -293,12 +316,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       ok = false;
       break;
     }
-    m = fmaxf(m, share_absmax<T>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), cw));
-    if (k + S < n) {  // tile k leaves shared memory: load tile k + S into its stage
-      finish_stage(s, [&] {
-        if (lane == 0) issue(k + S, k + S >= kept_from ? stream : keep);
-      });
-    }
+    const float mk = share_absmax<T>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), cw);
+    m = fmaxf(m, mk);
+    if (k + S < n)  // tile k leaves shared memory: load tile k + S into its stage
+      release_data(s, k + S, k + S >= kept_from ? stream : keep, __float_as_uint(mk));
   }
   if (!ok) *sm.abort_flag = 1;
 #pragma unroll
@@ -336,34 +357,80 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     sm.rtab_row[tid] = encode_factor((uint32_t)tid, g);
   else if (tid < 256)
     sm.rtab_col[tid - 128] = encode_factor((uint32_t)(tid - 128), g);
+  else if (tid < 256 + S) {  // the resident tile of each stage may stage its scales first
+    const int s = tid - 256;
+    sm.sc_owner[s] = s < n ? s + S * ((n - 1 - s) / S) : -1;
+  }
   __syncthreads();
 
-  // phase B: descending k, this group's tiles; the last warp done with a
-  // tile writes its scales back and reloads tile k - S into the stage
+  // phase B: descending k, this group's tiles.  A stage's data is released
+  // (tile k - S loaded into it) as soon as the group's warps have read their
+  // sub-tiles; its scale region is handed to tile k - S only after the last
+  // warp done with tile k has written tile k's scales back.
   const bool do_row = a.rowwise != 0, do_col = a.colwise != 0;
   const int k_top = n - 1 - ((n - 1 - grp) % kGroups + kGroups) % kGroups;  // largest k < n, k == grp mod kGroups
+  const volatile int* abort_flag = sm.abort_flag;
   for (int k = k_top; k >= 0; k -= kGroups) {
     const int s = k % S;
-    if (k < kept_from && !wait_full(k)) return;  // the waiting CTA gives up; outputs unfinished
+    if (*abort_flag) break;
+    if (k < kept_from && !wait_full(k)) {  // a wait ran out: outputs unfinished
+      *sm.abort_flag = 1;
+      break;
+    }
     int64_t r0, c0;
     tile_rc(k, r0, c0);
     uint8_t* sc = sm.sc + (size_t)s * 2 * kScRegion;
     const uint32_t st = smem_u32(sm.stages + (size_t)s * tile_bytes<T>());
-    if constexpr (sizeof(T) == 2)
+    if constexpr (sizeof(T) == 2) {
+      bool scales_ok = true;
+      const auto hooks = make_hooks([&](uint32_t token) { release_data(s, k - S, stream, token); },
+                                    [&] { scales_ok = wait_slot(&sm.sc_owner[s], k) && scales_ok; });
       wide_pass_any<MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, g,
-                          do_row, do_col, cw);
-    else
+                          do_row, do_col, cw, hooks);
+      if (!scales_ok) {  // a hand-over ran out: outputs unfinished
+        *sm.abort_flag = 1;
+        break;
+      }
+    } else {
       block_pass_any<T, MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g,
                               g, do_row, do_col, cw);
-    finish_stage(s, [&] {
+    }
+    // The last warp done with tile k writes its scales back; then (BF16)
+    // hands the scale region to tile k - S, or (FP32, whose data were read
+    // until now) loads tile k - S into the stage.
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = (atomicAdd(&sm.done[s], 1u) == (unsigned)(WPT - 1)) ? 1u : 0u;
+      if (last) {
+        sm.done[s] = 0;
+        __threadfence_block();
+      }
+    }
+    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+      __syncwarp();
       for (int t = lane; t < 128; t += 32) {
         if (do_row) store_scale_tile<MODE, false>(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
         if (do_col)
           store_scale_tile<MODE, true>(sc + kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
       }
       __syncwarp();
-      if (lane == 0 && k - S >= 0) issue(k - S, stream);
-    });
+      if (lane == 0) {
+        __threadfence_block();
+        if constexpr (sizeof(T) == 2)
+          *reinterpret_cast<volatile int*>(&sm.sc_owner[s]) = k - S;
+        else if (k - S >= 0)
+          issue(k - S, stream);
+      }
+    }
+  }
+  // After an abort, the last warp to leave lets the copies still in flight
+  // (the latest load into each stage) land, bounded, before the CTA exits.
+  __syncwarp();
+  if (lane == 0 && atomicAdd(&sm.exited[0], 1u) == (unsigned)(kWarps - 1) && *abort_flag) {
+    for (int s = 0; s < S; ++s)
+      if (sm.issued[s] > 0) mbar_wait_bounded(&sm.full[s], (sm.issued[s] - 1u) & 1u, a.status);
   }
 }
 

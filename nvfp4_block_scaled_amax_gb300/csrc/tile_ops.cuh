@@ -469,15 +469,26 @@ __device__ __forceinline__ uint32_t col_pair_acc_w(const uint32_t (&w)[8][4], in
   return xsa(xsa(xsa(w[0][p], w[1][p]), xsa(w[2][p], w[3][p])), xsa(xsa(w[4][p], w[5][p]), xsa(w[6][p], w[7][p])));
 }
 
+// No-op stage hooks (see wide_pass).
+struct NoHooks {
+  __device__ __forceinline__ void data_done(uint32_t) const {}
+  __device__ __forceinline__ void scale_wait() const {}
+};
+
 // Casts this lane's 8x16 sub-tile (wide mapping) of the staged tile at shared
 // address `stage`: stores its codes and stages its scales (staged_scale
 // layouts) at sc_row / sc_col.  `warp` is the warp's index (0..3) among the
 // four casting the tile.  kDirs: 3 both directions, 1 row-wise, 2
-// column-wise.  kInterior: the tile lies inside x.
-template <int MODE, int kDirs, bool kInterior>
+// column-wise.  kInterior: the tile lies inside x.  The warp calls
+// hooks.data_done(token) once its reads of the staged tile have completed
+// (token is computed from every word it read, so anything that depends on
+// it comes after those reads; the caller can then reuse the stage), and
+// hooks.scale_wait() before its first write to sc_row / sc_col.
+template <int MODE, int kDirs, bool kInterior, class Hooks = NoHooks>
 __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row, const float* rtab_col,
                                           uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
-                                          int64_t c0, float g_row, float g_col, int warp) {
+                                          int64_t c0, float g_row, float g_col, int warp,
+                                          const Hooks& hooks = Hooks()) {
   constexpr bool kRow = (kDirs & 1) != 0, kCol = (kDirs & 2) != 0;
   const int lane = threadIdx.x & 31;
   const int wr = warp >> 1, wc = warp & 1, i = lane >> 2, j = lane & 3, par = i & 1;
@@ -517,6 +528,7 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
       acc = xsa(acc, xsa(xsa(xsa(s.a[k][0], s.a[k][1]), xsa(s.a[k][2], s.a[k][3])),
                          xsa(xsa(s.b[k][0], s.b[k][1]), xsa(s.b[k][2], s.b[k][3]))));
     acc &= 0x7FFF7FFFu;
+    hooks.data_done(acc);  // every word of the sub-tile is in acc
     float m = fmaxf(bf16_lo(acc), bf16_hi(acc));
     m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
     const uint32_t sr = block_scale(m, g_row);
@@ -543,6 +555,7 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
         put_col(8 + c, par ? ca[c] : cb[c]);
       }
     }
+    hooks.scale_wait();
     if (par == 0) {
       const uint32_t o = (uint32_t)((trow >> 4) * 8 + (tcol >> 4));
       if (kRow) sts_u8(sc_row + o, sr);
@@ -574,6 +587,8 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
         pl[p >> 1] |= (sl0 | (sl1 << 8)) << (16 * (p & 1));
         pr[p >> 1] |= (sr0 | (sr1 << 8)) << (16 * (p & 1));
       }
+      if (!kRow) hooks.data_done(pl[0] ^ pl[1] ^ pr[0] ^ pr[1]);  // scales of every column
+      hooks.scale_wait();
       if (par == 0)  // lanes l and l ^ 4 hold the same column-block scales
         sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), pl[0], pl[1], pr[0], pr[1]);
     }
@@ -592,32 +607,34 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
         put_row(2 * t + 1, encode_half_row(s.a[2 * t + 1], f1), encode_half_row(s.b[2 * t + 1], f1));
         packed[t >> 1] |= (s0 | (s1 << 8)) << (16 * (t & 1));
       }
+      hooks.data_done(packed[0] ^ packed[1]);  // scales of every row
+      if (!kCol) hooks.scale_wait();
       sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
     }
   }
 }
 
-template <int MODE>
+template <int MODE, class Hooks = NoHooks>
 __device__ __forceinline__ void wide_pass_any(uint32_t stage, const float* rtab_row, const float* rtab_col,
                                               uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
                                               int64_t c0, float g_row, float g_col, bool do_row, bool do_col,
-                                              int warp) {
+                                              int warp, const Hooks& h = Hooks()) {
   const bool interior = (r0 + kTile <= a.M) && (c0 + kTile <= a.N);
   if (do_row && do_col) {
     if (interior)
-      wide_pass<MODE, 3, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+      wide_pass<MODE, 3, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
     else
-      wide_pass<MODE, 3, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+      wide_pass<MODE, 3, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
   } else if (do_row) {
     if (interior)
-      wide_pass<MODE, 1, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+      wide_pass<MODE, 1, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
     else
-      wide_pass<MODE, 1, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+      wide_pass<MODE, 1, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
   } else if (do_col) {
     if (interior)
-      wide_pass<MODE, 2, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+      wide_pass<MODE, 2, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
     else
-      wide_pass<MODE, 2, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
+      wide_pass<MODE, 2, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
   }
 }
 
