@@ -176,10 +176,11 @@ nvfp4_status nvfp4_quantize_rht(const void* x, int dtype, int64_t M, int64_t N,
  * directly in the GEMM layout.)
  *   workspace: NVFP4_SINGLE_PASS_WORKSPACE_BYTES of device memory, zeroed
  *   before its first use and not shared by calls that can run at the same
- *   time; the kernel leaves it ready for the next call (it holds a barrier
- *   generation, two arrival counts and one 4-byte partial maximum per CTA,
- *   one CTA per SM: up to 1008 SMs).  After a call that reported
- *   NVFP4_ERR_TIMEOUT through nvfp4_device_status, zero it again.
+ *   time; the kernel leaves it ready for the next call (it uses the first 64
+ *   bytes: the grid barrier's generation and, for two alternating
+ *   generations, an arrival count and a maximum; the rest is reserved).
+ *   After a call that reported NVFP4_ERR_TIMEOUT through
+ *   nvfp4_device_status, zero it again.
  *   flags: ROWWISE | COLWISE | SWIZZLED (no SKIP_AMAX: use the two-pass
  *   entry points for a given amax).  All CTAs must be co-resident (one per
  *   SM); a device where that is impossible returns NVFP4_ERR_CUDA.
@@ -196,7 +197,7 @@ nvfp4_status nvfp4_quantize_2d_single_pass(const void* x, int dtype, int64_t M, 
  * nvfp4_quantize_2d_single_pass for callers that cannot allocate device
  * memory.  This entry point has no counterpart on the pages this library
  * follows.  It computes exactly what nvfp4_quantize_2d_single_pass computes,
- * but takes no workspace: its scratch is a 1024-byte array inside the
+ * but takes no workspace: its scratch is a 256-byte array inside the
  * library that the CUDA runtime places on every GPU that loads it (held
  * until the process exits).  It serves callers with no device allocator of
  * their own (a plain C host embedding the library), callers on paths that
@@ -205,14 +206,14 @@ nvfp4_status nvfp4_quantize_2d_single_pass(const void* x, int dtype, int64_t M, 
  *   * The first call on a device looks up the array's device address (a
  *     runtime query, no allocation); make that first call before any stream
  *     capture on that device.
- *   * Every call clears the array's barrier header on `stream` (a memset)
- *     and then launches the kernel; it calls no cudaMalloc / cudaFree.
+ *   * Every call clears the array's 64-byte barrier header on `stream` (a
+ *     memset) and then launches the kernel; it calls no cudaMalloc /
+ *     cudaFree.
  *   * All calls on a device share the one array: calls that can overlap on
  *     the GPU (other streams, other threads) race and give wrong results;
  *     serialize them.
- *   * Limit: the kernel uses one CTA per SM, min(SMs, 128x128 tiles of x);
- *     the array holds one partial maximum for up to 240 CTAs.  A launch
- *     that would need more returns NVFP4_ERR_SHAPE (no GB300 does).
+ *   * Limit: the kernel needs the 64-byte header only, for any grid (one
+ *     CTA per SM), so the array's size bounds no input shape.
  * Arguments, flags and errors otherwise as nvfp4_quantize_2d_single_pass.
  */
 nvfp4_status nvfp4_quantize_2d_single_pass_noalloc(const void* x, int dtype, int64_t M, int64_t N,

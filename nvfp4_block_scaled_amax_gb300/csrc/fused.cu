@@ -52,7 +52,7 @@ struct FusedCfg<float> {
 template <typename T>
 __host__ __device__ constexpr size_t fused_smem_bytes() {
   return 1024 + (size_t)FusedCfg<T>::kStages * (tile_bytes<T>() + 2 * kScRegion) + 2 * 128 * 4 +
-         28 * FusedCfg<T>::kStages + 16 + 64 * 4 + 64;
+         28 * FusedCfg<T>::kStages + 16 + 64;
 }
 
 struct FSmem {
@@ -67,7 +67,7 @@ struct FSmem {
   int* tile_in;      // [S] tile index of the stage's latest issued load
   int* sc_owner;     // [S] tile allowed to write the stage's scale region
   unsigned* exited;  // [1] warps done with phase B
-  float* red;        // [64]
+  unsigned* gen;     // [1] this call's barrier generation
   float* amax;       // [1] broadcast of the global amax
   int* abort_flag;   // [1]
 };
@@ -105,8 +105,8 @@ __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
   s.tile_in = reinterpret_cast<int*>(s.issued + S);
   s.sc_owner = s.tile_in + S;
   s.exited = reinterpret_cast<unsigned*>(s.sc_owner + S);
-  s.red = reinterpret_cast<float*>(s.exited + 4);
-  s.amax = s.red + 64;
+  s.gen = s.exited + 1;
+  s.amax = reinterpret_cast<float*>(s.exited + 4);
   s.abort_flag = reinterpret_cast<int*>(s.amax + 1);
   return s;
 }
@@ -124,49 +124,42 @@ __device__ __forceinline__ void red_release_add_gpu(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Grid-wide maximum of one non-negative float per CTA, called by all threads
-// of every CTA.  Generation-counted, so the workspace needs no clearing
-// between calls: call g (read from ws->gen at the start) publishes its CTA
-// maxima in ws->slot[] and arrives on ws->count[g & 1]; every CTA polls the
-// count (bounded) and reduces the slots itself.  CTA 0 clears the other
-// count, which the next call uses, and advances the generation, which the
-// next call (ordered after this kernel) reads.  Returns false when the wait
-// ran out.  `red` is 32 floats of shared memory.
-__device__ bool grid_max(SinglePassWorkspace* ws, float m, unsigned n_cta, unsigned* status, float* red,
-                         float* out) {
-  __shared__ unsigned s_ok;
-  const unsigned tid = threadIdx.x;
-  if (tid == 0) {
-    const unsigned gen = ld_acquire_gpu(&ws->gen);
-    st_release_gpu(&ws->slot[blockIdx.x], __float_as_uint(m));
-    red_release_add_gpu(&ws->count[gen & 1u], 1u);
-    bool ok = true;
-    const long long t0 = clock64();
-    while (ld_acquire_gpu(&ws->count[gen & 1u]) < n_cta) {
-      if (clock64() - t0 > kWaitLimitCycles) {
-        atomicOr(status, kStatusGridTimeout);
-        ok = false;
-        break;
-      }
+__device__ __forceinline__ void red_relaxed_max_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier and maximum.  Generation-counted, so the workspace needs
+// no clearing between calls: call g (its generation read at kernel start)
+// uses the pair arrive[g & 1] / maxbits[g & 1].  Every warp of every CTA
+// publishes its maximum with a relaxed atomic max, then arrives with a
+// release add (which orders the max before it); thread 0 of each CTA polls
+// the count (acquire, bounded) and then reads the maximum.  CTA 0 clears the
+// other pair, which the next call uses, and advances the generation, which
+// the next call (ordered after this kernel) reads.
+__device__ __forceinline__ void grid_arrive(SinglePassWorkspace* ws, unsigned gen, float warp_max) {
+  red_relaxed_max_gpu(&ws->maxbits[gen & 1u], __float_as_uint(warp_max));
+  red_release_add_gpu(&ws->arrive[gen & 1u], 1u);
+}
+// Thread 0 only; false when the wait ran out.
+__device__ __forceinline__ bool grid_wait_max(SinglePassWorkspace* ws, unsigned gen, unsigned expected,
+                                              unsigned* status, float* out) {
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(&ws->arrive[gen & 1u]) < expected) {
+    if (clock64() - t0 > kWaitLimitCycles) {
+      atomicOr(status, kStatusGridTimeout);
+      return false;
     }
-    if (blockIdx.x == 0 && ok) {
-      ws->count[(gen + 1u) & 1u] = 0u;  // unused by this call; the next one counts there
-      st_release_gpu(&ws->gen, gen + 1u);
-    }
-    s_ok = ok ? 1u : 0u;
   }
-  __syncthreads();
-  if (!s_ok) return false;
-  float v = 0.0f;
-  for (unsigned c = tid; c < n_cta; c += blockDim.x) v = fmaxf(v, __uint_as_float(ld_acquire_gpu(&ws->slot[c])));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  if ((tid & 31) == 0) red[tid >> 5] = v;
-  __syncthreads();
-  if (tid == 0) {
-    float r = 0.0f;
-    for (unsigned w = 0; w < (blockDim.x >> 5); ++w) r = fmaxf(r, red[w]);
-    *out = r;
+  *out = __uint_as_float(ld_relaxed_gpu(&ws->maxbits[gen & 1u]));
+  if (blockIdx.x == 0) {  // unused by this call; the next one counts there
+    ws->arrive[(gen + 1u) & 1u] = 0u;
+    ws->maxbits[(gen + 1u) & 1u] = 0u;
+    st_release_gpu(&ws->gen, gen + 1u);
   }
   return true;
 }
@@ -238,6 +231,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                   pol);
   };
   if (tid == 0) {
+    *sm.gen = ld_acquire_gpu(&ws->gen);  // this call's barrier generation
     for (int s = 0; s < S; ++s) {
       mbar_init(&sm.full[s], 1);
       sm.done[s] = 0;
@@ -284,7 +278,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             good = 0;
             break;
           }
-          __nanosleep(64);
         }
       }
     }
@@ -324,19 +317,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   if (!ok) *sm.abort_flag = 1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  if (lane == 0) sm.red[warp] = m;
-  __syncthreads();
+  // Every warp arrives (a warp that lost a wait too, so the others are not
+  // held up); thread 0 waits for all of them.
+  const unsigned gen = *sm.gen;
+  if (lane == 0) grid_arrive(ws, gen, m);
   if (tid == 0) {
-    float cm = 0.0f;
-    for (int w = 0; w < kWarps; ++w) cm = fmaxf(cm, sm.red[w]);
-    sm.red[32] = cm;
-  }
-  __syncthreads();
-  // A CTA that lost a wait still arrives, so the others are not held up.
-  const bool gok = grid_max(ws, sm.red[32], (unsigned)G, a.status, sm.red, sm.amax);
-  if (tid == 0) {
+    float amax = 0.0f;
+    const bool gok = grid_wait_max(ws, gen, (unsigned)(kWarps * G), a.status, &amax);
     if (!gok) *sm.abort_flag = 1;
-    const float amax = *sm.amax;
     if (b == 0 && gok && !*sm.abort_flag) {
       if (a.amax_row) *const_cast<float*>(a.amax_row) = amax;
       if (a.amax_col) *const_cast<float*>(a.amax_col) = amax;
@@ -395,7 +383,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       block_pass_any<T, MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g,
                               g, do_row, do_col, cw);
     }
-    // The last warp done with tile k writes its scales back; then (BF16)
+    // The last warp done with tile k writes its scales back, then (BF16)
     // hands the scale region to tile k - S, or (FP32, whose data were read
     // until now) loads tile k - S into the stage.
     __syncwarp();
@@ -404,7 +392,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       __threadfence_block();
       last = (atomicAdd(&sm.done[s], 1u) == (unsigned)(WPT - 1)) ? 1u : 0u;
       if (last) {
-        sm.done[s] = 0;
+        sm.done[s] = 0;  // tile k - S counts only after the hand-over below
         __threadfence_block();
       }
     }
@@ -415,9 +403,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         if (do_col)
           store_scale_tile<MODE, true>(sc + kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
       }
-      __syncwarp();
+      __syncwarp();  // the lanes' reads of the scale region are complete (their stores used them)
       if (lane == 0) {
-        __threadfence_block();
         if constexpr (sizeof(T) == 2)
           *reinterpret_cast<volatile int*>(&sm.sc_owner[s]) = k - S;
         else if (k - S >= 0)

@@ -66,19 +66,20 @@ struct CastArgs {
 // launched as a programmatic dependent of the preceding amax kernel.
 cudaError_t launch_cast(const void* x, bool bf16, int mode, CastArgs args, bool pdl, const LaunchCtx& ctx);
 
-// Scratch of the single-pass kernels (zeroed before first use, then kept
-// consistent by the kernels themselves): the grid barrier's generation, the
-// arrival counts of the two alternating generations, and one partial
-// maximum per CTA.
+// Scratch of the single-pass kernels (a 64-byte header, zeroed before first
+// use, then kept consistent by the kernels themselves): the grid barrier's
+// generation, and for each of the two alternating generations the warps'
+// arrival count and the maximum they published (FP32 bits; non-negative
+// floats order like their bit patterns).
 struct SinglePassWorkspace {
   unsigned gen;
-  unsigned count[2];
-  unsigned pad[13];
-  unsigned slot[1];  // [grid]
+  unsigned pad0;
+  unsigned arrive[2];
+  unsigned maxbits[2];
+  unsigned pad[10];
 };
 constexpr size_t kSinglePassHeaderBytes = 64;
-// Most CTAs a workspace of `bytes` bytes can serve.
-constexpr int single_pass_max_ctas(size_t bytes) { return (int)((bytes - kSinglePassHeaderBytes) / 4); }
+static_assert(sizeof(SinglePassWorkspace) == kSinglePassHeaderBytes, "workspace header layout");
 
 // One persistent launch: per-tensor amax of x (written to args.amax_row /
 // args.amax_col) and the fused cast (1D or 2D), x read from HBM once.

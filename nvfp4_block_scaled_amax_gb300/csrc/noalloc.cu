@@ -1,9 +1,9 @@
 // noalloc.cu -- the single-pass 2D quantize for callers that cannot allocate
 // device memory.
 //
-// nvfp4_quantize_2d_single_pass needs a small workspace (a grid-barrier
-// generation, two arrival counts and one partial maximum per CTA) that the
-// caller normally allocates.  Some callers cannot do that: a plain C host
+// nvfp4_quantize_2d_single_pass needs a small workspace (the grid barrier's
+// 64-byte header: a generation, arrival counts and maxima) that the caller
+// normally allocates.  Some callers cannot do that: a plain C host
 // that embeds this library without any device memory manager, code on a
 // latency-critical path that must not take an allocator's lock or risk a
 // synchronizing cudaMalloc / cudaFree, or a process that sized all of its
@@ -18,9 +18,8 @@
 
 namespace {
 
-// The scratch: a 64-byte barrier header and one 4-byte partial maximum per
-// CTA (one CTA per SM), so 1024 bytes serve up to 240 SMs.
-constexpr size_t kScratchBytes = 1024;
+// The scratch: the kernel's 64-byte barrier header (any number of CTAs).
+constexpr size_t kScratchBytes = 256;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -28,7 +27,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 struct DeviceScratch {
   bool ready = false;
   void* ptr = nullptr;  // device address of g_noalloc_scratch on that device
-  int num_sms = 0;
 };
 DeviceScratch g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
@@ -36,7 +34,7 @@ std::mutex g_scratch_mu;
 // Once per device, with that device current: the device address of the
 // array.  In host code the symbol itself is only a host-side stand-in, never
 // a device address.
-nvfp4_status scratch_for_current_device(void** ptr, int* num_sms) {
+nvfp4_status scratch_for_current_device(void** ptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
@@ -44,14 +42,10 @@ nvfp4_status scratch_for_current_device(void** ptr, int* num_sms) {
   if (!d.ready) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return NVFP4_ERR_CUDA;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return NVFP4_ERR_CUDA;
     d.ptr = p;
-    d.num_sms = sms;
     d.ready = true;
   }
   *ptr = d.ptr;
-  *num_sms = d.num_sms;
   return NVFP4_OK;
 }
 
@@ -68,14 +62,10 @@ extern "C" nvfp4_status nvfp4_quantize_2d_single_pass_noalloc(const void* x, int
   nvfp4_status st = nvfp4::validate_single_pass(nvfp4::kCast2D, x, dtype, M, N, out, flags, noop);
   if (st != NVFP4_OK) return st;
   void* scratch = nullptr;
-  int num_sms = 0;
-  st = scratch_for_current_device(&scratch, &num_sms);
+  st = scratch_for_current_device(&scratch);
   if (st != NVFP4_OK) return st;
-  // One partial maximum per CTA must fit behind the header.
-  nvfp4::LaunchCtx ctx = {static_cast<cudaStream_t>(stream), num_sms, nullptr};
-  if (nvfp4::single_pass_grid(M, N, ctx) > nvfp4::single_pass_max_ctas(kScratchBytes)) return NVFP4_ERR_SHAPE;
   // The array keeps whatever the previous call left; the barrier header
-  // (generation and arrival counts) must start at zero, so clear it on the
+  // (generation, arrival counts, maxima) must start at zero, so clear it on the
   // stream before the kernel (a memset, no allocation).
   if (cudaMemsetAsync(scratch, 0, nvfp4::kSinglePassHeaderBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return NVFP4_ERR_CUDA;

@@ -46,15 +46,16 @@ __host__ __device__ constexpr int tile_bytes() {
 //     its sub-block's rows (row-wise) or columns (column-wise) for one scale
 //     column with one 8-byte store; the pitches (row-wise 160, column-wise
 //     192 bytes) put the eight-byte stores of a warp in distinct banks.
-//   * 2D: one byte per 16x16 tile, at (r / 16) * 8 + c row-wise and
-//     c * 8 + r / 16 column-wise (the same table: tile (ty, tx) at ty * 8 + tx).
+//   * 2D: one byte per 16x16 tile, at (r / 16) * 8 + c in both directions:
+//     tile (ty, tx) at ty * 8 + tx row-wise and at tx * 8 + ty column-wise,
+//     so that four consecutive scale columns of a row are one 32-bit word.
 constexpr int kScPitchRow = 160, kScPitchCol = 192;
 constexpr int kScRegion = 8 * kScPitchCol;  // bytes per direction
 
 template <int MODE, bool kColDir>
 __device__ __forceinline__ uint32_t staged_scale(const uint8_t* s, int r, int c) {
   if constexpr (MODE == kCast2D)
-    return kColDir ? s[c * 8 + (r >> 4)] : s[(r >> 4) * 8 + c];
+    return s[(r >> 4) * 8 + c];
   else
     return s[c * (kColDir ? kScPitchCol : kScPitchRow) + r];
 }
@@ -336,9 +337,8 @@ __device__ __forceinline__ void block_pass(uint32_t stage, const float* rtab_row
       for (int c = 0; c < 8; ++c) put_col(c, wc[c]);
     }
     if (stage_row && stage_col) {
-      const uint32_t o = (uint32_t)((trow >> 4) * 8 + (tcol >> 4));
-      if (kRow) sts_u8(sc_row + o, sr);
-      if (kCol) sts_u8(sc_col + o, sc);
+      if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sr);
+      if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sc);
     }
   } else {
     // 1D: row blocks 1x16 (lanes l, l^1), column blocks 16x1 (lanes l, l^8).
@@ -557,12 +557,16 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
     }
     hooks.scale_wait();
     if (par == 0) {
-      const uint32_t o = (uint32_t)((trow >> 4) * 8 + (tcol >> 4));
-      if (kRow) sts_u8(sc_row + o, sr);
-      if (kCol) sts_u8(sc_col + o, sc);
+      if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sr);
+      if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sc);
     }
   } else {
-    // column pass first, then the row pass: only the data stay live between them
+    // column pass first, then the row pass: only the data stay live between
+    // them.  Both directions: the column scales are staged after the row
+    // pass, so that the sub-tile's data are released (hooks.data_done)
+    // before the warp waits for the scale region (hooks.scale_wait), as on
+    // every other path.
+    uint32_t col_pl[2] = {0u, 0u}, col_pr[2] = {0u, 0u};
     if (kCol) {
       // column blocks span lanes l and l ^ 4, whose halves A are the other
       // side of the 16 columns: combine left with left, right with right
@@ -587,10 +591,13 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
         pl[p >> 1] |= (sl0 | (sl1 << 8)) << (16 * (p & 1));
         pr[p >> 1] |= (sr0 | (sr1 << 8)) << (16 * (p & 1));
       }
-      if (!kRow) hooks.data_done(pl[0] ^ pl[1] ^ pr[0] ^ pr[1]);  // scales of every column
-      hooks.scale_wait();
-      if (par == 0)  // lanes l and l ^ 4 hold the same column-block scales
-        sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), pl[0], pl[1], pr[0], pr[1]);
+      col_pl[0] = pl[0]; col_pl[1] = pl[1]; col_pr[0] = pr[0]; col_pr[1] = pr[1];
+      if (!kRow) {
+        hooks.data_done(pl[0] ^ pl[1] ^ pr[0] ^ pr[1]);  // scales of every column
+        hooks.scale_wait();
+        if (par == 0)  // lanes l and l ^ 4 hold the same column-block scales
+          sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), pl[0], pl[1], pr[0], pr[1]);
+      }
     }
     if (kRow) {
       // with both directions, re-read the sub-tile (still staged): keeping
@@ -608,7 +615,9 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
         packed[t >> 1] |= (s0 | (s1 << 8)) << (16 * (t & 1));
       }
       hooks.data_done(packed[0] ^ packed[1]);  // scales of every row
-      if (!kCol) hooks.scale_wait();
+      hooks.scale_wait();
+      if (kCol && par == 0)
+        sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), col_pl[0], col_pl[1], col_pr[0], col_pr[1]);
       sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
     }
   }
@@ -653,7 +662,7 @@ __device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out,
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) {
       const int r = 32 * qq + L;
-      if constexpr (MODE == kCast2D && !kColDir) {
+      if constexpr (MODE == kCast2D) {
         w[qq] = *reinterpret_cast<const uint32_t*>(s + (r >> 4) * 8 + 4 * h);
       } else {
         w[qq] = staged_scale<MODE, kColDir>(s, r, 4 * h) | (staged_scale<MODE, kColDir>(s, r, 4 * h + 1) << 8) |
@@ -670,7 +679,7 @@ __device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out,
     if (n <= 0) return;
     uint8_t* p = out + r * C + C0;
     uint32_t v[2];
-    if constexpr (MODE == kCast2D && !kColDir) {
+    if constexpr (MODE == kCast2D) {
       const uint2 u = *reinterpret_cast<const uint2*>(s + (t >> 4) * 8);
       v[0] = u.x;
       v[1] = u.y;

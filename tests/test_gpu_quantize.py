@@ -62,7 +62,8 @@ def test_single_pass_workspace_reuse(oracle_mod, mode):
             assert_quantize_equal(oracle_mod, q, ref, False, what=f"{mode} {M}x{N} call {it}")
     w = ws.view(torch.int32).cpu()
     assert int(w[0]) == 15 * 4                  # one generation per call
-    assert int(w[1 + (60 & 1)]) == 0            # the next call's arrival count is clear
+    assert int(w[2 + (60 & 1)]) == 0            # the next call's arrival count is clear
+    assert int(w[4 + (60 & 1)]) == 0            # and so is its maximum
     assert nv.device_status() == 0
 
 
