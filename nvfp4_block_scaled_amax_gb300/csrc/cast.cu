@@ -62,26 +62,30 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 }
 
 // ---------------------------------------------------------------------------
-// Hadamard column pass (BF16): warp w -> box w % 2, rows 32 (w / 2) .. +32;
-// lane l -> tile columns 64 (w % 2) + 2l, +1; two 16-row blocks per column,
-// each transformed as (1/4) H16 diag(sign) v and rounded to BF16 before its
-// amax, scale and codes.
+// Hadamard column pass (BF16): warp w -> box w % 2, rows 64 ((w / 2) % 2) ..
+// +64, box columns 32 (w / 4) .. +32; lane l -> columns 2 (l % 16), +1 of
+// those and rows 32 (l / 16) .. +32 of those.  Each column is two 16-row
+// blocks per lane, each transformed as (1/4) H16 diag(sign) v and rounded to
+// BF16 before its amax, scale and codes.  Lanes l and l + 16 hold the two
+// halves of 64 rows of a column: one 16-byte store each, together a whole
+// 32-byte sector of the column-wise output.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void rht_col_pass(const uint8_t* st, const Smem& sm, const CastArgs& a, int64_t r0,
                                              int64_t c0, float g_col, const float* sgn, int parity) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int box = warp & 1;
-  const int rbase = (warp >> 1) * 32;
+  const int box = warp & 1, li = lane & 15;
+  const int rbase = ((warp >> 1) & 1) * 64 + (lane >> 4) * 32;
+  const int cbox = (warp >> 2) * 32 + 2 * li;  // first of the lane's two columns within the box
   uint32_t w[32];
 #pragma unroll
   for (int r = 0; r < 32; ++r) {
     const int row = rbase + r;
-    w[r] = *reinterpret_cast<const uint32_t*>(st + swz(box, row, lane >> 2) + ((lane & 3) << 2));
+    w[r] = *reinterpret_cast<const uint32_t*>(st + swz(box, row, cbox >> 3) + ((cbox & 7) << 1));
   }
   const int64_t rg = r0 + rbase;
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
-    const int tcol = box * 64 + 2 * lane + cc;
+    const int tcol = box * 64 + cbox + cc;
     const int64_t x = c0 + tcol;
     uint32_t code[4];
 #pragma unroll

@@ -50,22 +50,28 @@ struct FusedCfg<float> {
 };
 
 template <typename T>
+__host__ __device__ constexpr int fused_groups() {
+  return kWarps / FusedCfg<T>::kWarpsPerTile;
+}
+// stages | per group two staged-scale buffers (row and column regions) |
+// encode-factor tables | mbarriers | stage and scale-buffer counters | misc
+template <typename T>
 __host__ __device__ constexpr size_t fused_smem_bytes() {
-  return 1024 + (size_t)FusedCfg<T>::kStages * (tile_bytes<T>() + 2 * kScRegion) + 2 * 128 * 4 +
-         28 * FusedCfg<T>::kStages + 16 + 64;
+  return 1024 + (size_t)FusedCfg<T>::kStages * tile_bytes<T>() + (size_t)fused_groups<T>() * 2 * 2 * kScRegion +
+         2 * 128 * 4 + 20 * FusedCfg<T>::kStages + 16 * fused_groups<T>() + 16 + 64;
 }
 
 struct FSmem {
   uint8_t* stages;   // [S][tile]
-  uint8_t* sc;       // [S][2][kScRegion] staged row / column scales of the tile in stage s
+  uint8_t* sc;       // [groups][2][2][kScRegion] staged row / column scales, two buffers per group
   float* rtab_row;   // [128]
   float* rtab_col;   // [128]
   uint64_t* full;    // [S]
-  unsigned* done;    // [S] warps done with the staged scales of the stage's tile
   unsigned* loaded;  // [S] warps done reading the stage's tile data
   unsigned* issued;  // [S] loads issued into the stage so far
   int* tile_in;      // [S] tile index of the stage's latest issued load
-  int* sc_owner;     // [S] tile allowed to write the stage's scale region
+  unsigned* staged;  // [groups][2] warps done staging into the buffer (all uses so far)
+  unsigned* wb;      // [groups][2] warps done writing the buffer's scales back (all uses so far)
   unsigned* exited;  // [1] warps done with phase B
   unsigned* gen;     // [1] this call's barrier generation
   float* amax;       // [1] broadcast of the global amax
@@ -95,16 +101,16 @@ __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
   s.stages = p;
   p += (size_t)S * tile_bytes<T>();
   s.sc = p;
-  p += (size_t)S * 2 * kScRegion;
+  p += (size_t)fused_groups<T>() * 2 * 2 * kScRegion;
   s.rtab_row = reinterpret_cast<float*>(p);
   s.rtab_col = s.rtab_row + 128;
   s.full = reinterpret_cast<uint64_t*>(s.rtab_col + 128);
-  s.done = reinterpret_cast<unsigned*>(s.full + S);
-  s.loaded = s.done + S;
+  s.loaded = reinterpret_cast<unsigned*>(s.full + S);
   s.issued = s.loaded + S;
   s.tile_in = reinterpret_cast<int*>(s.issued + S);
-  s.sc_owner = s.tile_in + S;
-  s.exited = reinterpret_cast<unsigned*>(s.sc_owner + S);
+  s.staged = reinterpret_cast<unsigned*>(s.tile_in + S);
+  s.wb = s.staged + 2 * fused_groups<T>();
+  s.exited = s.wb + 2 * fused_groups<T>();
   s.gen = s.exited + 1;
   s.amax = reinterpret_cast<float*>(s.exited + 4);
   s.abort_flag = reinterpret_cast<int*>(s.amax + 1);
@@ -234,11 +240,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     *sm.gen = ld_acquire_gpu(&ws->gen);  // this call's barrier generation
     for (int s = 0; s < S; ++s) {
       mbar_init(&sm.full[s], 1);
-      sm.done[s] = 0;
       sm.loaded[s] = 0;
       sm.issued[s] = 0;
       sm.tile_in[s] = -1;
-      sm.sc_owner[s] = -1;
+    }
+    for (int q = 0; q < 2 * kGroups; ++q) {
+      sm.staged[q] = 0;
+      sm.wb[q] = 0;
     }
     *sm.abort_flag = 0;
     *sm.exited = 0;
@@ -266,6 +274,26 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   };
   // Bounded wait of lane 0 until *slot == want (a shared-memory hand-over
   // between warps); false when it ran out.
+  // Bounded wait of lane 0 until the counter *p reaches `want`.
+  auto wait_count = [&](const unsigned* p, unsigned want) {
+    unsigned good = 1;
+    if (lane == 0) {
+      const volatile unsigned* c = p;
+      if (*c < want) {
+        const long long t0 = clock64();
+        while (*c < want) {
+          if (clock64() - t0 > kWaitLimitCycles) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            good = 0;
+            break;
+          }
+        }
+      }
+    }
+    const bool ok = __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
+    __threadfence_block();  // the counted warps' shared-memory writes are visible past this point
+    return ok;
+  };
   auto wait_slot = [&](const int* p, int want) {
     unsigned good = 1;
     if (lane == 0) {
@@ -345,20 +373,39 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     sm.rtab_row[tid] = encode_factor((uint32_t)tid, g);
   else if (tid < 256)
     sm.rtab_col[tid - 128] = encode_factor((uint32_t)(tid - 128), g);
-  else if (tid < 256 + S) {  // the resident tile of each stage may stage its scales first
-    const int s = tid - 256;
-    sm.sc_owner[s] = s < n ? s + S * ((n - 1 - s) / S) : -1;
-  }
   __syncthreads();
 
   // phase B: descending k, this group's tiles.  A stage's data is released
   // (tile k - S loaded into it) as soon as the group's warps have read their
-  // sub-tiles; its scale region is handed to tile k - S only after the last
-  // warp done with tile k has written tile k's scales back.
+  // sub-tiles.  Scales are staged in the group's own two buffers, used in
+  // turn; during its next tile each warp writes back its share of the
+  // previous tile's scales (waiting, bounded, until all the group's warps
+  // have staged them), and a buffer is reused only after every warp's share
+  // of its previous contents has been written back.
   const bool do_row = a.rowwise != 0, do_col = a.colwise != 0;
   const int k_top = n - 1 - ((n - 1 - grp) % kGroups + kGroups) % kGroups;  // largest k < n, k == grp mod kGroups
   const volatile int* abort_flag = sm.abort_flag;
-  for (int k = k_top; k >= 0; k -= kGroups) {
+  auto buffer = [&](int it) { return sm.sc + (size_t)((grp * 2 + (it & 1)) * 2) * kScRegion; };
+  // this warp's share of tile kk's (iteration it's) scale write-back
+  auto write_back_share = [&](int kk, int it) {
+    const int q = grp * 2 + (it & 1);
+    if (!wait_count(&sm.staged[q], (unsigned)(WPT * ((it >> 1) + 1)))) return false;
+    int64_t r0, c0;
+    tile_rc(kk, r0, c0);
+    const uint8_t* sc = buffer(it);
+    const int per = a.swizzled ? 64 / WPT : 128 / WPT;  // 16-byte lines or rows per warp
+    if (lane < per) {
+      const int t = cw * per + lane;
+      if (do_row) store_scale_tile<MODE, false>(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
+      if (do_col)
+        store_scale_tile<MODE, true>(sc + kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
+    }
+    __syncwarp();  // the lanes' reads of the buffer are complete (their stores used them)
+    if (lane == 0) atomicAdd(&sm.wb[q], 1u);
+    return true;
+  };
+  int it = 0, k_prev = -1;
+  for (int k = k_top; k >= 0; k -= kGroups, ++it) {
     const int s = k % S;
     if (*abort_flag) break;
     if (k < kept_from && !wait_full(k)) {  // a wait ran out: outputs unfinished
@@ -367,51 +414,40 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     int64_t r0, c0;
     tile_rc(k, r0, c0);
-    uint8_t* sc = sm.sc + (size_t)s * 2 * kScRegion;
+    uint8_t* sc = buffer(it);
     const uint32_t st = smem_u32(sm.stages + (size_t)s * tile_bytes<T>());
+    const unsigned* wbq = &sm.wb[grp * 2 + (it & 1)];
+    bool scales_ok = true;
+    // the buffer's previous contents (iteration it - 2) are written back
+    auto scale_wait = [&] { scales_ok = wait_count(wbq, (unsigned)(WPT * (it >> 1))) && scales_ok; };
     if constexpr (sizeof(T) == 2) {
-      bool scales_ok = true;
-      const auto hooks = make_hooks([&](uint32_t token) { release_data(s, k - S, stream, token); },
-                                    [&] { scales_ok = wait_slot(&sm.sc_owner[s], k) && scales_ok; });
+      const auto hooks = make_hooks([&](uint32_t token) { release_data(s, k - S, stream, token); }, scale_wait);
       wide_pass_any<MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, g,
                           do_row, do_col, cw, hooks);
-      if (!scales_ok) {  // a hand-over ran out: outputs unfinished
-        *sm.abort_flag = 1;
-        break;
-      }
     } else {
+      scale_wait();
       block_pass_any<T, MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g,
                               g, do_row, do_col, cw);
-    }
-    // The last warp done with tile k writes its scales back, then (BF16)
-    // hands the scale region to tile k - S, or (FP32, whose data were read
-    // until now) loads tile k - S into the stage.
-    __syncwarp();
-    unsigned last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = (atomicAdd(&sm.done[s], 1u) == (unsigned)(WPT - 1)) ? 1u : 0u;
-      if (last) {
-        sm.done[s] = 0;  // tile k - S counts only after the hand-over below
-        __threadfence_block();
-      }
-    }
-    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
       __syncwarp();
-      for (int t = lane; t < 128; t += 32) {
-        if (do_row) store_scale_tile<MODE, false>(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
-        if (do_col)
-          store_scale_tile<MODE, true>(sc + kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
-      }
-      __syncwarp();  // the lanes' reads of the scale region are complete (their stores used them)
-      if (lane == 0) {
-        if constexpr (sizeof(T) == 2)
-          *reinterpret_cast<volatile int*>(&sm.sc_owner[s]) = k - S;
-        else if (k - S >= 0)
-          issue(k - S, stream);
-      }
+      __threadfence_block();  // the warp's reads of the stage are done
+      release_data(s, k - S, stream, 0u);
     }
+    if (!scales_ok) {  // a wait ran out: outputs unfinished
+      *sm.abort_flag = 1;
+      break;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();  // this warp's staged scales before its count
+      atomicAdd(&sm.staged[grp * 2 + (it & 1)], 1u);
+    }
+    if (k_prev >= 0 && !write_back_share(k_prev, it - 1)) {
+      *sm.abort_flag = 1;
+      break;
+    }
+    k_prev = k;
   }
+  if (k_prev >= 0 && !*abort_flag && !write_back_share(k_prev, it - 1)) *sm.abort_flag = 1;
   // After an abort, the last warp to leave lets the copies still in flight
   // (the latest load into each stage) land, bounded, before the CTA exits.
   __syncwarp();
