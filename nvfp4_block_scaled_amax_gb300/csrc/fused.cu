@@ -49,6 +49,10 @@ struct FusedCfg<float> {
   static constexpr int kWarpsPerTile = 8;  // 8x8 sub-blocks
 };
 
+// Phase A keeps the 16x16 maxima of the tiles of each CTA (2D, BF16, up to
+// kPreTiles tiles per CTA), so that phase B need not find them again.
+constexpr int kPreTiles = 32;
+
 template <typename T>
 __host__ __device__ constexpr int fused_groups() {
   return kWarps / FusedCfg<T>::kWarpsPerTile;
@@ -58,7 +62,8 @@ __host__ __device__ constexpr int fused_groups() {
 template <typename T>
 __host__ __device__ constexpr size_t fused_smem_bytes() {
   return 1024 + (size_t)FusedCfg<T>::kStages * tile_bytes<T>() + (size_t)fused_groups<T>() * 2 * 2 * kScRegion +
-         2 * 128 * 4 + 20 * FusedCfg<T>::kStages + 16 * fused_groups<T>() + 16 + 64;
+         2 * 128 * 4 + 20 * FusedCfg<T>::kStages + 16 * fused_groups<T>() + 16 + 64 +
+         (sizeof(T) == 2 ? kPreTiles * 64 * 2 : 0);
 }
 
 struct FSmem {
@@ -76,6 +81,7 @@ struct FSmem {
   unsigned* gen;     // [1] this call's barrier generation
   float* amax;       // [1] broadcast of the global amax
   int* abort_flag;   // [1]
+  uint16_t* pre;     // [kPreTiles][64] 2D (BF16): 16x16 tile maxima found in phase A
 };
 
 // The two stage hooks the cast passes call (see wide_pass).
@@ -83,13 +89,16 @@ template <class D, class W>
 struct StageHooksT {
   D done_fn;
   W wait_fn;
+  const uint16_t* pre;  // 2D: the tile's 16x16 maxima found in phase A, or null
   __device__ __forceinline__ void data_done(uint32_t token) const { done_fn(token); }
   __device__ __forceinline__ void scale_wait() const { wait_fn(); }
+  __device__ __forceinline__ const uint16_t* tile_max() const { return pre; }
 };
 template <class D, class W>
-__device__ __forceinline__ StageHooksT<D, W> make_hooks(D d, W w) {
-  return StageHooksT<D, W>{d, w};
+__device__ __forceinline__ StageHooksT<D, W> make_hooks(D d, W w, const uint16_t* pre = nullptr) {
+  return StageHooksT<D, W>{d, w, pre};
 }
+
 
 template <typename T>
 __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
@@ -114,6 +123,7 @@ __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
   s.gen = s.exited + 1;
   s.amax = reinterpret_cast<float*>(s.exited + 4);
   s.abort_flag = reinterpret_cast<int*>(s.amax + 1);
+  s.pre = reinterpret_cast<uint16_t*>(s.abort_flag + 1);
   return s;
 }
 
@@ -330,6 +340,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   };
 
   // phase A: max|x| of this group's tiles (k == grp mod kGroups)
+  constexpr bool kPre = MODE == kCast2D && sizeof(T) == 2;
+  const bool use_pre = kPre && n <= kPreTiles;
   float m = 0.0f;
   for (int k = grp; k < n; k += kGroups) {
     const int s = k % S;
@@ -337,7 +349,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       ok = false;
       break;
     }
-    const float mk = share_absmax<T>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), cw);
+    float mk;
+    if (use_pre) {
+      // the wide partition of phase B: record the tile's 16x16 maxima
+      SubW sw;
+      const int wr = cw >> 1, wc = cw & 1, i = lane >> 2, j = lane & 3;
+      load_sub_w(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), wc, 64 * wr + 8 * i, j, i & 1, sw);
+      uint32_t acc;
+      mk = wide_tile_max(sw.a, sw.b, acc);
+      if ((i & 1) == 0) sm.pre[k * 64 + (4 * wr + (i >> 1)) * 8 + 4 * wc + j] = (uint16_t)(__float_as_uint(mk) >> 16);
+    } else {
+      mk = share_absmax<T>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), cw);
+    }
     m = fmaxf(m, mk);
     if (k + S < n)  // tile k leaves shared memory: load tile k + S into its stage
       release_data(s, k + S, k + S >= kept_from ? stream : keep, __float_as_uint(mk));
@@ -421,7 +444,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // the buffer's previous contents (iteration it - 2) are written back
     auto scale_wait = [&] { scales_ok = wait_count(wbq, (unsigned)(WPT * (it >> 1))) && scales_ok; };
     if constexpr (sizeof(T) == 2) {
-      const auto hooks = make_hooks([&](uint32_t token) { release_data(s, k - S, stream, token); }, scale_wait);
+      const auto hooks = make_hooks([&](uint32_t token) { release_data(s, k - S, stream, token); }, scale_wait,
+                                    use_pre ? sm.pre + k * 64 : nullptr);
       wide_pass_any<MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, g,
                           do_row, do_col, cw, hooks);
     } else {

@@ -473,7 +473,24 @@ __device__ __forceinline__ uint32_t col_pair_acc_w(const uint32_t (&w)[8][4], in
 struct NoHooks {
   __device__ __forceinline__ void data_done(uint32_t) const {}
   __device__ __forceinline__ void scale_wait() const {}
+  __device__ __forceinline__ const uint16_t* tile_max() const { return nullptr; }
 };
+
+// 2D: max|x| of the 16x16 tile this lane's wide sub-tile belongs to (this
+// lane's 128 values and lane l ^ 4's), as a packed BF16 pair with both
+// halves non-negative; `acc_out` gets the lane's own packed maximum.
+__device__ __forceinline__ float wide_tile_max(const uint32_t (&a)[8][4], const uint32_t (&b)[8][4],
+                                               uint32_t& acc_out) {
+  uint32_t acc = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    acc = xsa(acc, xsa(xsa(xsa(a[k][0], a[k][1]), xsa(a[k][2], a[k][3])),
+                       xsa(xsa(b[k][0], b[k][1]), xsa(b[k][2], b[k][3]))));
+  acc &= 0x7FFF7FFFu;
+  acc_out = acc;
+  const float m = fmaxf(bf16_lo(acc), bf16_hi(acc));
+  return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+}
 
 // Casts this lane's 8x16 sub-tile (wide mapping) of the staged tile at shared
 // address `stage`: stores its codes and stages its scales (staged_scale
@@ -483,7 +500,9 @@ struct NoHooks {
 // hooks.data_done(token) once its reads of the staged tile have completed
 // (token is computed from every word it read, so anything that depends on
 // it comes after those reads; the caller can then reuse the stage), and
-// hooks.scale_wait() before its first write to sc_row / sc_col.
+// hooks.scale_wait() before its first write to sc_row / sc_col.  In 2D,
+// hooks.tile_max() may give the tile's 16x16 maxima (BF16 bits, [ty][tx])
+// found while the tile was first read; else they are computed here.
 template <int MODE, int kDirs, bool kInterior, class Hooks = NoHooks>
 __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row, const float* rtab_col,
                                           uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
@@ -521,20 +540,19 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
   };
 
   if constexpr (MODE == kCast2D) {
-    // 16x16 tile: this lane's 128 values and lane l ^ 4's
-    uint32_t acc = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      acc = xsa(acc, xsa(xsa(xsa(s.a[k][0], s.a[k][1]), xsa(s.a[k][2], s.a[k][3])),
-                         xsa(xsa(s.b[k][0], s.b[k][1]), xsa(s.b[k][2], s.b[k][3]))));
-    acc &= 0x7FFF7FFFu;
-    hooks.data_done(acc);  // every word of the sub-tile is in acc
-    float m = fmaxf(bf16_lo(acc), bf16_hi(acc));
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    const uint16_t* pre = hooks.tile_max();
+    float m;
+    if (pre != nullptr) {
+      m = __uint_as_float((uint32_t)pre[(trow >> 4) * 8 + (tcol >> 4)] << 16);
+    } else {
+      uint32_t acc;
+      m = wide_tile_max(s.a, s.b, acc);
+      hooks.data_done(acc);  // every word of the sub-tile is in acc
+    }
     const uint32_t sr = block_scale(m, g_row);
     const uint32_t sc = (g_col == g_row) ? sr : block_scale(m, g_col);
     const float rr = rtab_row[sr], rc = rtab_col[sc];
-    uint32_t ca[8], cb[8];
+    uint32_t ca[8], cb[8], tok = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const uint32_t wa = encode_half_row(s.a[k], kRow ? rr : rc);
@@ -545,7 +563,9 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
         ca[k] = same ? wa : encode_half_row(s.a[k], rc);
         cb[k] = same ? wb : encode_half_row(s.b[k], rc);
       }
+      if (pre != nullptr) tok ^= wa ^ wb;
     }
+    if (pre != nullptr) hooks.data_done(tok);  // each row's codes depend on its words
     if (kCol) {
       transpose_nibbles8x8(ca);
       transpose_nibbles8x8(cb);
