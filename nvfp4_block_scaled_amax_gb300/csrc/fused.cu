@@ -79,6 +79,8 @@ struct FSmem {
   unsigned* wb;      // [groups][2] warps done writing the buffer's scales back (all uses so far)
   unsigned* exited;  // [1] warps done with phase B
   unsigned* gen;     // [1] this call's barrier generation
+  unsigned* cta_max; // [1] the CTA's max|x| bits (phase A)
+  unsigned* cta_in;  // [1] warps done with phase A
   float* amax;       // [1] broadcast of the global amax
   int* abort_flag;   // [1]
   uint16_t* pre;     // [kPreTiles][64] 2D (BF16): 16x16 tile maxima found in phase A
@@ -121,6 +123,8 @@ __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
   s.wb = s.staged + 2 * fused_groups<T>();
   s.exited = s.wb + 2 * fused_groups<T>();
   s.gen = s.exited + 1;
+  s.cta_max = s.exited + 2;
+  s.cta_in = s.exited + 3;
   s.amax = reinterpret_cast<float*>(s.exited + 4);
   s.abort_flag = reinterpret_cast<int*>(s.amax + 1);
   s.pre = reinterpret_cast<uint16_t*>(s.abort_flag + 1);
@@ -151,12 +155,13 @@ __device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
 
 // Grid-wide barrier and maximum.  Generation-counted, so the workspace needs
 // no clearing between calls: call g (its generation read at kernel start)
-// uses the pair arrive[g & 1] / maxbits[g & 1].  Every warp of every CTA
-// publishes its maximum with a relaxed atomic max, then arrives with a
-// release add (which orders the max before it); thread 0 of each CTA polls
-// the count (acquire, bounded) and then reads the maximum.  CTA 0 clears the
-// other pair, which the next call uses, and advances the generation, which
-// the next call (ordered after this kernel) reads.
+// uses the pair arrive[g & 1] / maxbits[g & 1].  The last warp of each CTA
+// to finish phase A (a shared-memory count) publishes the CTA's maximum with
+// a relaxed atomic max, then arrives with a release add (which orders the
+// max before it); thread 0 of each CTA polls the count (acquire, bounded)
+// and then reads the maximum.  CTA 0 clears the other pair, which the next
+// call uses, and advances the generation, which the next call (ordered after
+// this kernel) reads.
 __device__ __forceinline__ void grid_arrive(SinglePassWorkspace* ws, unsigned gen, float warp_max) {
   red_relaxed_max_gpu(&ws->maxbits[gen & 1u], __float_as_uint(warp_max));
   red_release_add_gpu(&ws->arrive[gen & 1u], 1u);
@@ -260,6 +265,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     *sm.abort_flag = 0;
     *sm.exited = 0;
+    *sm.cta_max = 0;
+    *sm.cta_in = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap);
     for (int k = 0; k < S && k < n; ++k) issue(k, k >= kept_from ? stream : keep);
@@ -368,13 +375,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   if (!ok) *sm.abort_flag = 1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  // Every warp arrives (a warp that lost a wait too, so the others are not
-  // held up); thread 0 waits for all of them.
+  // Every warp counts in (a warp that lost a wait too, so the others are not
+  // held up); the CTA's last one arrives at the grid barrier for the CTA;
+  // thread 0 waits for all CTAs.
   const unsigned gen = *sm.gen;
-  if (lane == 0) grid_arrive(ws, gen, m);
+  if (lane == 0) {
+    atomicMax(sm.cta_max, __float_as_uint(m));
+    __threadfence_block();
+    if (atomicAdd(sm.cta_in, 1u) == (unsigned)(kWarps - 1)) {
+      __threadfence_block();
+      grid_arrive(ws, gen, __uint_as_float(*reinterpret_cast<volatile unsigned*>(sm.cta_max)));
+    }
+  }
   if (tid == 0) {
     float amax = 0.0f;
-    const bool gok = grid_wait_max(ws, gen, (unsigned)(kWarps * G), a.status, &amax);
+    const bool gok = grid_wait_max(ws, gen, (unsigned)G, a.status, &amax);
     if (!gok) *sm.abort_flag = 1;
     if (b == 0 && gok && !*sm.abort_flag) {
       if (a.amax_row) *const_cast<float*>(a.amax_row) = amax;
