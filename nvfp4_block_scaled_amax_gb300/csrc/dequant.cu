@@ -34,6 +34,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// A thread handles four 16-element blocks per step, consecutive threads on
+// consecutive blocks; the codes and scales of all four are loaded before any
+// is decoded, so that enough loads are in flight to cover the memory latency.
+constexpr int kDeqUnroll = 4;
+
 template <bool kOutBF16>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t* __restrict__ data,
                                                            const uint8_t* __restrict__ scale,
@@ -45,31 +50,45 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t* __rest
   const int64_t C = cols / 16;
   const int64_t nblk = rows * C;
   const float a0 = row_scaled ? 0.0f : amax[0];
-  for (int64_t b = (int64_t)blockIdx.x * kThreads + threadIdx.x; b < nblk; b += (int64_t)gridDim.x * kThreads) {
-    const int64_t y = b / C, k = b - y * C;
-    const uint2 q = *reinterpret_cast<const uint2*>(data + y * (cols / 2) + 8 * k);
-    const uint32_t s = scale[swizzled ? swizzled_scale_offset(y, k, C) : b];
-    const float a = row_scaled ? amax[y] : a0;
-    const float kf = __fdiv_rn(a, 2688.0f);
-    const float sv = e4m3_decode(s);
-    float o[16];
+  const int64_t T = (int64_t)gridDim.x * kThreads;
+  for (int64_t b0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; b0 < nblk; b0 += kDeqUnroll * T) {
+    uint2 q[kDeqUnroll];
+    uint32_t sc[kDeqUnroll];
+    float kf[kDeqUnroll];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t code = ((i < 8 ? q.x : q.y) >> (4 * (i & 7))) & 0xFu;
-      o[i] = __fmul_rn(__fmul_rn(lut[code], sv), kf);
+    for (int u = 0; u < kDeqUnroll; ++u) {
+      const int64_t b = b0 + u * T;
+      if (b < nblk) {
+        const int64_t y = b / C, k = b - y * C;
+        q[u] = *reinterpret_cast<const uint2*>(data + y * (cols / 2) + 8 * k);
+        sc[u] = scale[swizzled ? swizzled_scale_offset(y, k, C) : b];
+        kf[u] = __fdiv_rn(row_scaled ? amax[y] : a0, 2688.0f);
+      }
     }
-    if constexpr (kOutBF16) {
-      uint8_t* dst = static_cast<uint8_t*>(out) + (y * cols + 16 * k) * 2;
-      st_cs_v4(dst, pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
-               pack_bf16x2(o[6], o[7]));
-      st_cs_v4(dst + 16, pack_bf16x2(o[8], o[9]), pack_bf16x2(o[10], o[11]), pack_bf16x2(o[12], o[13]),
-               pack_bf16x2(o[14], o[15]));
-    } else {
-      uint8_t* dst = static_cast<uint8_t*>(out) + (y * cols + 16 * k) * 4;
 #pragma unroll
-      for (int v = 0; v < 4; ++v)
-        st_cs_v4(dst + 16 * v, __float_as_uint(o[4 * v]), __float_as_uint(o[4 * v + 1]),
-                 __float_as_uint(o[4 * v + 2]), __float_as_uint(o[4 * v + 3]));
+    for (int u = 0; u < kDeqUnroll; ++u) {
+      const int64_t b = b0 + u * T;
+      if (b >= nblk) break;
+      const float sv = e4m3_decode(sc[u]);
+      float o[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t code = ((i < 8 ? q[u].x : q[u].y) >> (4 * (i & 7))) & 0xFu;
+        o[i] = __fmul_rn(__fmul_rn(lut[code], sv), kf[u]);
+      }
+      if constexpr (kOutBF16) {
+        uint8_t* dst = static_cast<uint8_t*>(out) + b * 32;  // block b = elements 16 b .. 16 b + 15
+        st_cs_v4(dst, pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                 pack_bf16x2(o[6], o[7]));
+        st_cs_v4(dst + 16, pack_bf16x2(o[8], o[9]), pack_bf16x2(o[10], o[11]), pack_bf16x2(o[12], o[13]),
+                 pack_bf16x2(o[14], o[15]));
+      } else {
+        uint8_t* dst = static_cast<uint8_t*>(out) + b * 64;
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          st_cs_v4(dst + 16 * v, __float_as_uint(o[4 * v]), __float_as_uint(o[4 * v + 1]),
+                   __float_as_uint(o[4 * v + 2]), __float_as_uint(o[4 * v + 3]));
+      }
     }
   }
 }

@@ -6,6 +6,7 @@
 // the warp makes an amax pass and re-reads the row (from L1/L2) to cast it.
 #include "common.cuh"
 #include "kernels.h"
+#include "tile_ops.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -37,10 +38,17 @@ __device__ __forceinline__ float vec_elem(const uint4* v, int i) {
 
 template <bool kBF16>
 __device__ __forceinline__ float block_absmax(const uint4* v) {
-  float m = 0.0f;
+  if constexpr (kBF16) {  // packed BF16 pairs
+    const uint32_t acc = tile::xsa(tile::xsa(tile::xsa(v[0].x, v[0].y), tile::xsa(v[0].z, v[0].w)),
+                                   tile::xsa(tile::xsa(v[1].x, v[1].y), tile::xsa(v[1].z, v[1].w))) &
+                         0x7FFF7FFFu;
+    return fmaxf(bf16_lo(acc), bf16_hi(acc));
+  } else {
+    float m = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(vec_elem<kBF16>(v, i)));
-  return m;
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(vec_elem<kBF16>(v, i)));
+    return m;
+  }
 }
 
 template <bool kBF16>
@@ -48,18 +56,27 @@ __device__ __forceinline__ void cast_block(const uint4* v, float bmax, float g, 
                                            uint8_t* data, uint8_t* scale, bool swizzled) {
   const uint32_t s = e4m3_rn_satfinite(__fmul_rn(div6_rn(bmax), g));
   const float r = encode_factor(s, g);
-  float e[16];
+  uint32_t lo, hi;
+  if constexpr (kBF16) {  // packed FP32x2 products straight from the BF16 words
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
+    lo = tile::encode8(bf16_lo(w[0]), bf16_hi(w[0]), bf16_lo(w[1]), bf16_hi(w[1]), bf16_lo(w[2]), bf16_hi(w[2]),
+                       bf16_lo(w[3]), bf16_hi(w[3]), r);
+    hi = tile::encode8(bf16_lo(w[4]), bf16_hi(w[4]), bf16_lo(w[5]), bf16_hi(w[5]), bf16_lo(w[6]), bf16_hi(w[6]),
+                       bf16_lo(w[7]), bf16_hi(w[7]), r);
+  } else {
+    float e[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) e[i] = __fmul_rn(vec_elem<kBF16>(v, i), r);
-  const uint32_t lo = e2m1x8(e[0], e[1], e[2], e[3], e[4], e[5], e[6], e[7]);
-  const uint32_t hi = e2m1x8(e[8], e[9], e[10], e[11], e[12], e[13], e[14], e[15]);
+    for (int i = 0; i < 16; ++i) e[i] = __fmul_rn(vec_elem<kBF16>(v, i), r);
+    lo = e2m1x8(e[0], e[1], e[2], e[3], e[4], e[5], e[6], e[7]);
+    hi = e2m1x8(e[8], e[9], e[10], e[11], e[12], e[13], e[14], e[15]);
+  }
   st_cs_v2(data + y * (N / 2) + 8 * k, lo, hi);
   const int64_t C = N / 16;
   st_cs_u8(scale + (swizzled ? swizzled_scale_offset(y, k, C) : y * C + k), s);
 }
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kThreads) row_scaled_kernel(const void* __restrict__ x, int64_t M, int64_t N,
+__global__ void __launch_bounds__(kThreads, 2) row_scaled_kernel(const void* __restrict__ x, int64_t M, int64_t N,
                                                               uint8_t* data, uint8_t* scale, float* amax,
                                                               int skip_amax, int swizzled, const float* noop) {
   using RC = RowCfg<kBF16>;
@@ -77,7 +94,6 @@ __global__ void __launch_bounds__(kThreads) row_scaled_kernel(const void* __rest
     if (nseg <= 1) {
       // Whole row in registers: one HBM read.
       uint4 v[RC::kBPL][RC::kV];
-      float bm[RC::kBPL];
 #pragma unroll
       for (int j = 0; j < RC::kBPL; ++j) {
         const int64_t k = (int64_t)j * 32 + lane;
@@ -87,10 +103,7 @@ __global__ void __launch_bounds__(kThreads) row_scaled_kernel(const void* __rest
       }
       float m = 0.0f;
 #pragma unroll
-      for (int j = 0; j < RC::kBPL; ++j) {
-        bm[j] = block_absmax<kBF16>(v[j]);
-        m = fmaxf(m, bm[j]);
-      }
+      for (int j = 0; j < RC::kBPL; ++j) m = fmaxf(m, block_absmax<kBF16>(v[j]));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
       if (skip_amax)
@@ -101,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) row_scaled_kernel(const void* __rest
 #pragma unroll
       for (int j = 0; j < RC::kBPL; ++j) {
         const int64_t k = (int64_t)j * 32 + lane;
-        if (k < nblk) cast_block<kBF16>(v[j], bm[j], g, y, k, N, data, scale, swizzled);
+        if (k < nblk) cast_block<kBF16>(v[j], block_absmax<kBF16>(v[j]), g, y, k, N, data, scale, swizzled);
       }
     } else {
       // Long row: amax pass, then a second read that casts.
