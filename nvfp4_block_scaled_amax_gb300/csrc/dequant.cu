@@ -34,10 +34,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// A thread handles four 16-element blocks per step, consecutive threads on
-// consecutive blocks; the codes and scales of all four are loaded before any
-// is decoded, so that enough loads are in flight to cover the memory latency.
-constexpr int kDeqUnroll = 4;
+// A warp walks the rows (one row at a time, rows spread over the grid's
+// warps): each step covers 16 blocks of the row as 32 half blocks, lane l
+// taking half (l & 1) of block (l >> 1) -- 4 code bytes in, 8 outputs out.
+// The warp's code loads are then 128 contiguous bytes and, for BF16 output,
+// its stores 512 contiguous bytes (whole 32-byte sectors).  Four steps are
+// loaded before any is decoded, to keep enough loads in flight.
+constexpr int kDeqSteps = 4;
 
 template <bool kOutBF16>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t* __restrict__ data,
@@ -48,46 +51,41 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t* __rest
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_decode(threadIdx.x);
   __syncthreads();
   const int64_t C = cols / 16;
-  const int64_t nblk = rows * C;
-  const float a0 = row_scaled ? 0.0f : amax[0];
-  const int64_t T = (int64_t)gridDim.x * kThreads;
-  for (int64_t b0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; b0 < nblk; b0 += kDeqUnroll * T) {
-    uint2 q[kDeqUnroll];
-    uint32_t sc[kDeqUnroll];
-    float kf[kDeqUnroll];
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int half = lane & 1;
+  for (int64_t y = warp0; y < rows; y += nwarps) {
+    const float kf = __fdiv_rn(row_scaled ? amax[y] : amax[0], 2688.0f);
+    const uint8_t* drow = data + y * (cols / 2);
+    for (int64_t k0 = 0; k0 < C; k0 += 16 * kDeqSteps) {
+      uint32_t q[kDeqSteps], sc[kDeqSteps];
 #pragma unroll
-    for (int u = 0; u < kDeqUnroll; ++u) {
-      const int64_t b = b0 + u * T;
-      if (b < nblk) {
-        const int64_t y = b / C, k = b - y * C;
-        q[u] = *reinterpret_cast<const uint2*>(data + y * (cols / 2) + 8 * k);
-        sc[u] = scale[swizzled ? swizzled_scale_offset(y, k, C) : b];
-        kf[u] = __fdiv_rn(row_scaled ? amax[y] : a0, 2688.0f);
+      for (int u = 0; u < kDeqSteps; ++u) {
+        const int64_t k = k0 + 16 * u + (lane >> 1);
+        if (k < C) {
+          q[u] = *reinterpret_cast<const uint32_t*>(drow + 8 * k + 4 * half);
+          sc[u] = scale[swizzled ? swizzled_scale_offset(y, k, C) : y * C + k];
+        }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kDeqUnroll; ++u) {
-      const int64_t b = b0 + u * T;
-      if (b >= nblk) break;
-      const float sv = e4m3_decode(sc[u]);
-      float o[16];
+      for (int u = 0; u < kDeqSteps; ++u) {
+        const int64_t k = k0 + 16 * u + (lane >> 1);
+        if (k >= C) break;
+        const float sv = e4m3_decode(sc[u]);
+        float o[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t code = ((i < 8 ? q[u].x : q[u].y) >> (4 * (i & 7))) & 0xFu;
-        o[i] = __fmul_rn(__fmul_rn(lut[code], sv), kf[u]);
-      }
-      if constexpr (kOutBF16) {
-        uint8_t* dst = static_cast<uint8_t*>(out) + b * 32;  // block b = elements 16 b .. 16 b + 15
-        st_cs_v4(dst, pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
-                 pack_bf16x2(o[6], o[7]));
-        st_cs_v4(dst + 16, pack_bf16x2(o[8], o[9]), pack_bf16x2(o[10], o[11]), pack_bf16x2(o[12], o[13]),
-                 pack_bf16x2(o[14], o[15]));
-      } else {
-        uint8_t* dst = static_cast<uint8_t*>(out) + b * 64;
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          st_cs_v4(dst + 16 * v, __float_as_uint(o[4 * v]), __float_as_uint(o[4 * v + 1]),
-                   __float_as_uint(o[4 * v + 2]), __float_as_uint(o[4 * v + 3]));
+        for (int i = 0; i < 8; ++i) o[i] = __fmul_rn(__fmul_rn(lut[(q[u] >> (4 * i)) & 0xFu], sv), kf);
+        const int64_t e0 = y * cols + 16 * k + 8 * half;  // first output element
+        if constexpr (kOutBF16) {
+          st_cs_v4(static_cast<uint8_t*>(out) + e0 * 2, pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                   pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+        } else {
+          uint8_t* dst = static_cast<uint8_t*>(out) + e0 * 4;
+          st_cs_v4(dst, __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+          st_cs_v4(dst + 16, __float_as_uint(o[4]), __float_as_uint(o[5]), __float_as_uint(o[6]),
+                   __float_as_uint(o[7]));
+        }
       }
     }
   }
@@ -118,7 +116,7 @@ cudaError_t launch_dequantize(const uint8_t* data, const uint8_t* scale, const f
                               const LaunchCtx& ctx) {
   const int64_t nblk = rows * (cols / 16);
   if (nblk == 0) return cudaSuccess;
-  const int grid = grid_for(nblk, ctx.num_sms);
+  const int grid = grid_for(rows * 32, ctx.num_sms);  // a warp per row at a time
   if (out_bf16)
     dequant_kernel<true><<<grid, kThreads, 0, ctx.stream>>>(data, scale, amax, rows, cols, swizzled, row_scaled,
                                                             out);
