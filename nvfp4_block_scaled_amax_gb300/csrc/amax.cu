@@ -123,10 +123,10 @@ constexpr int kRhtAmaxThreads = 256;
 // One work item = 16 rows x 8 columns (one 16-byte vector per row): row
 // max|x| over the 128 values and, per column, max|(1/4) H16 diag(sign) v|.
 // Consecutive threads take consecutive 8-column chunks (512 contiguous
-// bytes per row and warp).  The column maximum is rounded to BF16 once per
-// block before the atomic: rounding is monotone, so this equals the maximum
-// of the rounded transform outputs.
-__global__ void __launch_bounds__(kRhtAmaxThreads) rht_amax_kernel(const uint16_t* __restrict__ x, int64_t M,
+// bytes per row and warp).  Two columns go through the transform together as
+// FP32x2 pairs; each output is rounded to BF16 (as the cast rounds it) and
+// the maxima are kept as packed BF16 pairs.
+__global__ void __launch_bounds__(kRhtAmaxThreads, 2) rht_amax_kernel(const uint16_t* __restrict__ x, int64_t M,
                                                                    int64_t N, uint32_t sign_mask, float* a_row,
                                                                    float* a_col, const float* noop) {
   __shared__ float red[kRhtAmaxThreads / 32];
@@ -138,8 +138,7 @@ __global__ void __launch_bounds__(kRhtAmaxThreads) rht_amax_kernel(const uint16_
   const int64_t chunks = N / 8;
   const int64_t items = (M / 16) * chunks;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  uint32_t racc = 0;
-  float cmax = 0.0f;
+  uint32_t racc = 0, cacc = 0;
   for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += stride) {
     const int64_t band = it / chunks, chunk = it - band * chunks;
     const uint4* base = reinterpret_cast<const uint4*>(x + (band * 16) * N + chunk * 8);
@@ -156,22 +155,24 @@ __global__ void __launch_bounds__(kRhtAmaxThreads) rht_amax_kernel(const uint16_
       asm("max.bf16x2 %0, %0, %1;" : "+r"(racc) : "r"(t1));
     }
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float u[16];
+    for (int q = 0; q < 4; ++q) {  // columns 2q and 2q + 1 as FP32x2 pairs
+      uint64_t u[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        const uint32_t w = (c < 2) ? v[r].x : (c < 4) ? v[r].y : (c < 6) ? v[r].z : v[r].w;
-        const float e = (c & 1) ? bf16_hi(w) : bf16_lo(w);
-        u[r] = __fmul_rn(e, sgn[r]);
+        const uint32_t w = (q == 0) ? v[r].x : (q == 1) ? v[r].y : (q == 2) ? v[r].z : v[r].w;
+        u[r] = bf16x2_scaled(w, sgn[r]);
       }
-      fwht16(u);
+      fwht16_x2(u);
 #pragma unroll
-      for (int o = 0; o < 16; ++o) cmax = fmaxf(cmax, fabsf(u[o]));
+      for (int o = 0; o < 16; ++o) {
+        uint32_t h = pair_to_bf16x2(u[o]) & 0x7FFF7FFFu;
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(cacc) : "r"(h));
+      }
     }
   }
   float rm = block_max(bf16x2_hmax_to_f32(racc), red);
   __syncthreads();
-  float cm = block_max(round_bf16(cmax), red);
+  float cm = block_max(bf16x2_hmax_to_f32(cacc), red);
   if (threadIdx.x == 0) {
     grid_dependency_wait();
     if (a_row != nullptr) atomicMax(reinterpret_cast<int*>(a_row), __float_as_int(rm));

@@ -83,41 +83,54 @@ __device__ __forceinline__ void rht_col_pass(const uint8_t* st, const Smem& sm, 
     w[r] = *reinterpret_cast<const uint32_t*>(st + swz(box, row, cbox >> 3) + ((cbox & 7) << 1));
   }
   const int64_t rg = r0 + rbase;
+  // The lane's two columns travel together as FP32x2 pairs (column cbox in
+  // the low half): packed sign products and butterflies, one BF16x2
+  // rounding per row, packed block maxima; each column keeps its own scale.
+  uint32_t code[2][4];  // [column][16-row block pair of words]
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    uint64_t v[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) v[r] = bf16x2_scaled(w[16 * blk + r], sgn[r]);
+    fwht16_x2(v);
+    uint32_t hb[16];  // BF16x2 of the transformed row: column cbox low, cbox + 1 high
+    uint32_t acc = 0;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      hb[r] = pair_to_bf16x2(v[r]);
+      acc = xsa(acc, hb[r]);
+    }
+    acc &= 0x7FFF7FFFu;
+    const uint32_t s0 = block_scale(bf16_lo(acc), g_col), s1 = block_scale(bf16_hi(acc), g_col);
+    const uint64_t rr = mul2(sm.rtab_col[s0], sm.rtab_col[s1], splat2(1.0f));
+    float p[16][2];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const uint64_t pr = mul2(bf16_lo(hb[r]), bf16_hi(hb[r]), rr);
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(p[r][0]), "=f"(p[r][1]) : "l"(pr));
+    }
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      code[cc][2 * blk] = e2m1x8(p[0][cc], p[1][cc], p[2][cc], p[3][cc], p[4][cc], p[5][cc], p[6][cc], p[7][cc]);
+      code[cc][2 * blk + 1] =
+          e2m1x8(p[8][cc], p[9][cc], p[10][cc], p[11][cc], p[12][cc], p[13][cc], p[14][cc], p[15][cc]);
+    }
+    const int tcol = box * 64 + cbox;
+    sm.sc_col[parity * kScRegion + ((rbase >> 4) + blk) * kScPitchCol + tcol] = (uint8_t)s0;
+    sm.sc_col[parity * kScRegion + ((rbase >> 4) + blk) * kScPitchCol + tcol + 1] = (uint8_t)s1;
+  }
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
-    const int tcol = box * 64 + cbox + cc;
-    const int64_t x = c0 + tcol;
-    uint32_t code[4];
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-      float v[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const uint32_t word = w[16 * blk + r];
-        v[r] = __fmul_rn(cc ? bf16_hi(word) : bf16_lo(word), sgn[r]);
-      }
-      fwht16(v);
-      float bm = 0.0f;
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        v[r] = round_bf16(v[r]);
-        bm = fmaxf(bm, fabsf(v[r]));
-      }
-      const uint32_t s = block_scale(bm, g_col);
-      const float rf = sm.rtab_col[s];
-      code[2 * blk] = encode8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], rf);
-      code[2 * blk + 1] = encode8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15], rf);
-      sm.sc_col[parity * kScRegion + ((rbase >> 4) + blk) * kScPitchCol + tcol] = (uint8_t)s;
-    }
+    const int64_t x = c0 + box * 64 + cbox + cc;
     // M % 16 == 0: the first block is inside when rg < M, the second when
     // rg + 16 < M.
     if (x < a.N && rg < a.M) {
       uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
       if (rg + 32 <= a.M && ((a.M / 2) & 15) == 0) {
-        st_cs_v4(dst, code[0], code[1], code[2], code[3]);
+        st_cs_v4(dst, code[cc][0], code[cc][1], code[cc][2], code[cc][3]);
       } else {
-        st_cs_v2(dst, code[0], code[1]);
-        if (rg + 16 < a.M) st_cs_v2(dst + 8, code[2], code[3]);
+        st_cs_v2(dst, code[cc][0], code[cc][1]);
+        if (rg + 16 < a.M) st_cs_v2(dst + 8, code[cc][2], code[cc][3]);
       }
     }
   }

@@ -132,6 +132,38 @@ __device__ __forceinline__ void fwht16(float* v) {
   }
 }
 
+// The same transform on two columns at once, each value an FP32x2 pair
+// (packed adds and subtracts round each half exactly as the scalar ones).
+__device__ __forceinline__ void fwht16_x2(uint64_t* v) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const uint64_t a = v[i], c = v[i + h];
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(v[i]) : "l"(a), "l"(c));
+        asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(v[i + h]) : "l"(a), "l"(c));
+      }
+    }
+  }
+}
+// BF16x2 word -> FP32x2 pair times (r, r).
+__device__ __forceinline__ uint64_t bf16x2_scaled(uint32_t w, float r) {
+  uint64_t p, v, rr;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(rr) : "f"(r));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(v), "l"(rr));
+  return p;
+}
+// FP32x2 pair -> BF16x2 word (RNE), low half from the pair's low value.
+__device__ __forceinline__ uint32_t pair_to_bf16x2(uint64_t v) {
+  float lo, hi;
+  uint32_t w;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+  return w;
+}
+
 // ---------------------------------------------------------------------------
 // Shared memory, mbarrier and TMA
 // ---------------------------------------------------------------------------
