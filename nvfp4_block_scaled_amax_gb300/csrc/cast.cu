@@ -212,11 +212,11 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
     // this tile's scales: threads 0..127 row-wise, 128..255 column-wise
     if (tid < 128) {
       if (do_row)
-        store_scale_tile<MODE, false>(sm.sc_row + parity * kScRegion, a.scale_row, r0, c0 / 16, a.M, a.N / 16,
-                                      a.swizzled, tid);
+        store_scale_tile<MODE, false>(smem_u32(sm.sc_row + parity * kScRegion), a.scale_row, r0, c0 / 16, a.M,
+                                      a.N / 16, a.swizzled, tid);
     } else if (a.colwise) {
-      store_scale_tile<MODE, true>(sm.sc_col + parity * kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16,
-                                   a.swizzled, tid - 128);
+      store_scale_tile<MODE, true>(smem_u32(sm.sc_col + parity * kScRegion), a.scale_col, c0, r0 / 16, a.N,
+                                   a.M / 16, a.swizzled, tid - 128);
     }
   }
   if (k < my_count && tid == 0) {

@@ -52,12 +52,31 @@ __host__ __device__ constexpr int tile_bytes() {
 constexpr int kScPitchRow = 160, kScPitchCol = 192;
 constexpr int kScRegion = 8 * kScPitchCol;  // bytes per direction
 
+// Explicit shared-memory loads of staged scales (a generic load could alias
+// global memory, so it would be ordered behind the warp's pending stores).
+// The "memory" clobber keeps them after the waits that publish the scales.
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
 template <int MODE, bool kColDir>
-__device__ __forceinline__ uint32_t staged_scale(const uint8_t* s, int r, int c) {
+__device__ __forceinline__ uint32_t staged_scale(uint32_t s, int r, int c) {
   if constexpr (MODE == kCast2D)
-    return s[(r >> 4) * 8 + c];
+    return lds_u8(s + (uint32_t)((r >> 4) * 8 + c));
   else
-    return s[c * (kColDir ? kScPitchCol : kScPitchRow) + r];
+    return lds_u8(s + (uint32_t)(c * (kColDir ? kScPitchCol : kScPitchRow) + r));
 }
 
 // stages | 2 encode-factor tables | 2 x 2 staged scale regions | barriers | flag
@@ -492,21 +511,33 @@ __device__ __forceinline__ float wide_tile_max(const uint32_t (&a)[8][4], const 
   return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
 }
 
+// Byte offset, in a tile's staged atoms of the 128x4 layout, of the word of
+// scale row `r` (0..127: a tile row for row-wise scales, a tile column for
+// column-wise ones) in atom `h` (0, 1: column blocks 4h..4h+3 of that row):
+// 16-byte line r & 31, word r >> 5.
+__device__ __forceinline__ uint32_t stage_swz_offset(int r, int h) {
+  return (uint32_t)(h * 512 + (r & 31) * 16 + (r >> 5) * 4);
+}
+
 // Casts this lane's 8x16 sub-tile (wide mapping) of the staged tile at shared
 // address `stage`: stores its codes and stages its scales (staged_scale
 // layouts) at sc_row / sc_col.  `warp` is the warp's index (0..3) among the
-// four casting the tile.  kDirs: 3 both directions, 1 row-wise, 2
-// column-wise.  kInterior: the tile lies inside x.  The warp calls
+// four casting the tile.  Both directions share the global encode scale g
+// (the amax is per tensor) and its table rtab[s] = encode factor of scale
+// code s.  kDirs: 3 both directions, 1 row-wise, 2 column-wise.
+// kInterior: the tile lies inside x.  The warp calls
 // hooks.data_done(token) once its reads of the staged tile have completed
 // (token is computed from every word it read, so anything that depends on
 // it comes after those reads; the caller can then reuse the stage), and
 // hooks.scale_wait() before its first write to sc_row / sc_col.  In 2D,
 // hooks.tile_max() may give the tile's 16x16 maxima (BF16 bits, [ty][tx])
 // found while the tile was first read; else they are computed here.
-template <int MODE, int kDirs, bool kInterior, class Hooks = NoHooks>
-__device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row, const float* rtab_col,
-                                          uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
-                                          int64_t c0, float g_row, float g_col, int warp,
+// kSwz (tiles inside x, 128x4 layout): the scales are staged as the tile's
+// two 512-byte atoms per direction, byte for byte as they are stored (see
+// stage_swz_offset), so that one bulk copy per direction writes them.
+template <int MODE, int kDirs, bool kInterior, bool kSwz = false, class Hooks = NoHooks>
+__device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uint32_t sc_row, uint32_t sc_col,
+                                          const CastArgs& a, int64_t r0, int64_t c0, float g, int warp,
                                           const Hooks& hooks = Hooks()) {
   constexpr bool kRow = (kDirs & 1) != 0, kCol = (kDirs & 2) != 0;
   const int lane = threadIdx.x & 31;
@@ -549,20 +580,18 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
       m = wide_tile_max(s.a, s.b, acc);
       hooks.data_done(acc);  // every word of the sub-tile is in acc
     }
-    const uint32_t sr = block_scale(m, g_row);
-    const uint32_t sc = (g_col == g_row) ? sr : block_scale(m, g_col);
-    const float rr = rtab_row[sr], rc = rtab_col[sc];
+    // one scale and one set of codes serve both directions (the column-wise
+    // codes are the row-wise ones transposed)
+    const uint32_t sb = block_scale(m, g);
+    const float rf = rtab[sb];
     uint32_t ca[8], cb[8], tok = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t wa = encode_half_row(s.a[k], kRow ? rr : rc);
-      const uint32_t wb = encode_half_row(s.b[k], kRow ? rr : rc);
+      const uint32_t wa = encode_half_row(s.a[k], rf);
+      const uint32_t wb = encode_half_row(s.b[k], rf);
       if (kRow) put_row(k, wa, wb);
-      if (kCol) {
-        const bool same = !kRow || rc == rr;
-        ca[k] = same ? wa : encode_half_row(s.a[k], rc);
-        cb[k] = same ? wb : encode_half_row(s.b[k], rc);
-      }
+      ca[k] = wa;
+      cb[k] = wb;
       if (pre != nullptr) tok ^= wa ^ wb;
     }
     if (pre != nullptr) hooks.data_done(tok);  // each row's codes depend on its words
@@ -575,10 +604,26 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
         put_col(8 + c, par ? ca[c] : cb[c]);
       }
     }
-    hooks.scale_wait();
-    if (par == 0) {
-      if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sr);
-      if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sc);
+    if constexpr (kSwz) {
+      // the four column blocks of a row (lanes j) and the four row blocks of
+      // a column (lanes i >> 1) gathered into the 4-byte word they share
+      uint32_t wrow = sb << (8 * j), wcol = sb << (8 * (i >> 1));
+      wrow |= __shfl_xor_sync(0xFFFFFFFFu, wrow, 1);
+      wrow |= __shfl_xor_sync(0xFFFFFFFFu, wrow, 2);
+      wcol |= __shfl_xor_sync(0xFFFFFFFFu, wcol, 8);
+      wcol |= __shfl_xor_sync(0xFFFFFFFFu, wcol, 16);
+      hooks.scale_wait();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {  // rows trow + 2j + t; columns tcol + 2i + t
+        if (kRow) sts_u32(sc_row + stage_swz_offset(trow + 2 * j + t, tcol >> 6), wrow);
+        if (kCol) sts_u32(sc_col + stage_swz_offset(tcol + 2 * i + t, trow >> 6), wcol);
+      }
+    } else {
+      hooks.scale_wait();
+      if (par == 0) {
+        if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sb);
+        if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sb);
+      }
     }
   } else {
     // column pass first, then the row pass: only the data stay live between
@@ -587,6 +632,19 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
     // before the warp waits for the scale region (hooks.scale_wait), as on
     // every other path.
     uint32_t col_pl[2] = {0u, 0u}, col_pr[2] = {0u, 0u};
+    // lanes l and l ^ 4 hold the same column-block scales: the lanes with
+    // par == 0 stage them (byte c of left / right: column tcol + c / + 8 + c)
+    auto stage_col = [&] {
+      if constexpr (kSwz) {
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const uint32_t w = (cc < 8 ? col_pl : col_pr)[(cc & 7) >> 2];
+          sts_u8(sc_col + stage_swz_offset(tcol + cc, trow >> 6) + ((trow >> 4) & 3), w >> (8 * (cc & 3)));
+        }
+      } else {
+        sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), col_pl[0], col_pl[1], col_pr[0], col_pr[1]);
+      }
+    };
     if (kCol) {
       // column blocks span lanes l and l ^ 4, whose halves A are the other
       // side of the 16 columns: combine left with left, right with right
@@ -597,9 +655,9 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
         uint32_t ml = par ? xb : xa, mr = par ? xa : xb;
         ml = xsa(ml, __shfl_xor_sync(0xFFFFFFFFu, ml, 4)) & 0x7FFF7FFFu;
         mr = xsa(mr, __shfl_xor_sync(0xFFFFFFFFu, mr, 4)) & 0x7FFF7FFFu;
-        const uint32_t sl0 = block_scale(bf16_lo(ml), g_col), sl1 = block_scale(bf16_hi(ml), g_col);
-        const uint32_t sr0 = block_scale(bf16_lo(mr), g_col), sr1 = block_scale(bf16_hi(mr), g_col);
-        const float fl0 = rtab_col[sl0], fl1 = rtab_col[sl1], fr0 = rtab_col[sr0], fr1 = rtab_col[sr1];
+        const uint32_t sl0 = block_scale(bf16_lo(ml), g), sl1 = block_scale(bf16_hi(ml), g);
+        const uint32_t sr0 = block_scale(bf16_lo(mr), g), sr1 = block_scale(bf16_hi(mr), g);
+        const float fl0 = rtab[sl0], fl1 = rtab[sl1], fr0 = rtab[sr0], fr1 = rtab[sr1];
         const uint32_t wa0 = encode_half_col(s.a, 2 * p, par ? fr0 : fl0);
         const uint32_t wa1 = encode_half_col(s.a, 2 * p + 1, par ? fr1 : fl1);
         const uint32_t wb0 = encode_half_col(s.b, 2 * p, par ? fl0 : fr0);
@@ -615,8 +673,7 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
       if (!kRow) {
         hooks.data_done(pl[0] ^ pl[1] ^ pr[0] ^ pr[1]);  // scales of every column
         hooks.scale_wait();
-        if (par == 0)  // lanes l and l ^ 4 hold the same column-block scales
-          sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), pl[0], pl[1], pr[0], pr[1]);
+        if (par == 0) stage_col();
       }
     }
     if (kRow) {
@@ -628,42 +685,57 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab_row,
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const uint32_t pr = row_pair_max_w(s, 2 * t, 2 * t + 1);
-        const uint32_t s0 = block_scale(bf16_lo(pr), g_row), s1 = block_scale(bf16_hi(pr), g_row);
-        const float f0 = rtab_row[s0], f1 = rtab_row[s1];
+        const uint32_t s0 = block_scale(bf16_lo(pr), g), s1 = block_scale(bf16_hi(pr), g);
+        const float f0 = rtab[s0], f1 = rtab[s1];
         put_row(2 * t, encode_half_row(s.a[2 * t], f0), encode_half_row(s.b[2 * t], f0));
         put_row(2 * t + 1, encode_half_row(s.a[2 * t + 1], f1), encode_half_row(s.b[2 * t + 1], f1));
         packed[t >> 1] |= (s0 | (s1 << 8)) << (16 * (t & 1));
       }
       hooks.data_done(packed[0] ^ packed[1]);  // scales of every row
       hooks.scale_wait();
-      if (kCol && par == 0)
-        sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), col_pl[0], col_pl[1], col_pr[0], col_pr[1]);
-      sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
+      if (kCol && par == 0) stage_col();
+      if constexpr (kSwz) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          sts_u8(sc_row + stage_swz_offset(trow + k, tcol >> 6) + j, packed[k >> 2] >> (8 * (k & 3)));
+      } else {
+        sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
+      }
     }
   }
 }
 
+// wide_pass for the directions and tile position at hand; `swz_stage`
+// (tiles inside x): stage the scales in the 128x4 layout's byte order.
 template <int MODE, class Hooks = NoHooks>
-__device__ __forceinline__ void wide_pass_any(uint32_t stage, const float* rtab_row, const float* rtab_col,
-                                              uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
-                                              int64_t c0, float g_row, float g_col, bool do_row, bool do_col,
-                                              int warp, const Hooks& h = Hooks()) {
+__device__ __forceinline__ void wide_pass_any(uint32_t stage, const float* rtab, uint32_t sc_row, uint32_t sc_col,
+                                              const CastArgs& a, int64_t r0, int64_t c0, float g, bool do_row,
+                                              bool do_col, int warp, bool swz_stage, const Hooks& h = Hooks()) {
+  if (swz_stage) {
+    if (do_row && do_col)
+      wide_pass<MODE, 3, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
+    else if (do_row)
+      wide_pass<MODE, 1, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
+    else if (do_col)
+      wide_pass<MODE, 2, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
+    return;
+  }
   const bool interior = (r0 + kTile <= a.M) && (c0 + kTile <= a.N);
   if (do_row && do_col) {
     if (interior)
-      wide_pass<MODE, 3, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
+      wide_pass<MODE, 3, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
     else
-      wide_pass<MODE, 3, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
+      wide_pass<MODE, 3, false>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
   } else if (do_row) {
     if (interior)
-      wide_pass<MODE, 1, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
+      wide_pass<MODE, 1, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
     else
-      wide_pass<MODE, 1, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
+      wide_pass<MODE, 1, false>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
   } else if (do_col) {
     if (interior)
-      wide_pass<MODE, 2, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
+      wide_pass<MODE, 2, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
     else
-      wide_pass<MODE, 2, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp, h);
+      wide_pass<MODE, 2, false>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
   }
 }
 
@@ -671,7 +743,7 @@ __device__ __forceinline__ void wide_pass_any(uint32_t stage, const float* rtab_
 // for tile rows R0 .. R0 + 127 and scale columns C0 .. C0 + 7 of an R x C
 // scale matrix; t = 0..127.
 template <int MODE, bool kColDir>
-__device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out, int64_t R0, int64_t C0, int64_t R,
+__device__ __forceinline__ void store_scale_tile(uint32_t s, uint8_t* out, int64_t R0, int64_t C0, int64_t R,
                                                  int64_t C, bool swizzled, int t) {
   if (swizzled) {
     // Two 512-byte tiles of the 128x4 layout, contiguous (R, C aligned):
@@ -683,7 +755,7 @@ __device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out,
     for (int qq = 0; qq < 4; ++qq) {
       const int r = 32 * qq + L;
       if constexpr (MODE == kCast2D) {
-        w[qq] = *reinterpret_cast<const uint32_t*>(s + (r >> 4) * 8 + 4 * h);
+        w[qq] = lds_u32(s + (uint32_t)((r >> 4) * 8 + 4 * h));
       } else {
         w[qq] = staged_scale<MODE, kColDir>(s, r, 4 * h) | (staged_scale<MODE, kColDir>(s, r, 4 * h + 1) << 8) |
                 (staged_scale<MODE, kColDir>(s, r, 4 * h + 2) << 16) |
@@ -700,7 +772,7 @@ __device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out,
     uint8_t* p = out + r * C + C0;
     uint32_t v[2];
     if constexpr (MODE == kCast2D) {
-      const uint2 u = *reinterpret_cast<const uint2*>(s + (t >> 4) * 8);
+      const uint2 u = lds_v2(s + (uint32_t)((t >> 4) * 8));
       v[0] = u.x;
       v[1] = u.y;
     } else {
