@@ -101,7 +101,7 @@ __device__ __forceinline__ void rht_col_pass(const uint8_t* st, const Smem& sm, 
       acc = xsa(acc, hb[r]);
     }
     acc &= 0x7FFF7FFFu;
-    const uint32_t s0 = block_scale(bf16_lo(acc), g_col), s1 = block_scale(bf16_hi(acc), g_col);
+    const uint32_t s01 = block_scale2(bf16_lo(acc), bf16_hi(acc), g_col), s0 = s01 & 0xFFu, s1 = s01 >> 8;
     const uint64_t rr = mul2(sm.rtab_col[s0], sm.rtab_col[s1], splat2(1.0f));
     float p[16][2];
 #pragma unroll

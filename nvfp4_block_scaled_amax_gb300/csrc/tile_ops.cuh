@@ -96,6 +96,30 @@ __device__ __forceinline__ uint32_t swz(int box, int row, int chunk) {
 __device__ __forceinline__ uint32_t block_scale(float b, float g) {
   return e4m3_rn_satfinite(__fmul_rn(div6_rn(b), g));
 }
+// block_scale of two block maxima at once (packed FP32x2 arithmetic, one
+// E4M3 pair conversion): s(b0) | s(b1) << 8.  The same steps as div6_rn
+// (quotient, exact residual, correction; tiny maxima take the division).
+__device__ __forceinline__ uint32_t block_scale2(float b0, float b1, float g) {
+  float v0, v1;
+  if (fminf(b0, b1) < 1.0e-30f) {
+    v0 = __fmul_rn(div6_rn(b0), g);
+    v1 = __fmul_rn(div6_rn(b1), g);
+  } else {
+    uint64_t b, q, e, c, m6, gg;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(c) : "f"(1.0f / 6.0f));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(m6) : "f"(-6.0f));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(gg) : "f"(g));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(b), "l"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q), "l"(m6), "l"(b));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(c), "l"(q));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(q), "l"(gg));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v0), "=f"(v1) : "l"(q));
+  }
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(v1), "f"(v0));
+  return h;
+}
 
 // Two products in one packed FP32x2 multiply (each an IEEE product rounded
 // to nearest), then the E2M1 codes of eight values.
@@ -374,7 +398,7 @@ __device__ __forceinline__ void block_pass(uint32_t stage, const float* rtab_row
           m0 = row_max_f32(s, 2 * t);
           m1 = row_max_f32(s, 2 * t + 1);
         }
-        const uint32_t s0 = block_scale(m0, g_row), s1 = block_scale(m1, g_row);
+        const uint32_t s01 = block_scale2(m0, m1, g_row), s0 = s01 & 0xFFu, s1 = s01 >> 8;
         put_row(2 * t, encode_row<T>(s, 2 * t, rtab_row[s0]));
         put_row(2 * t + 1, encode_row<T>(s, 2 * t + 1, rtab_row[s1]));
         packed[t >> 1] |= (s0 | (s1 << 8)) << (16 * (t & 1));
@@ -394,7 +418,7 @@ __device__ __forceinline__ void block_pass(uint32_t stage, const float* rtab_row
           m0 = col_max_f32(s, 2 * p);
           m1 = col_max_f32(s, 2 * p + 1);
         }
-        const uint32_t s0 = block_scale(m0, g_col), s1 = block_scale(m1, g_col);
+        const uint32_t s01 = block_scale2(m0, m1, g_col), s0 = s01 & 0xFFu, s1 = s01 >> 8;
         put_col(2 * p, encode_col<T>(s, 2 * p, rtab_col[s0]));
         put_col(2 * p + 1, encode_col<T>(s, 2 * p + 1, rtab_col[s1]));
         packed[p >> 1] |= (s0 | (s1 << 8)) << (16 * (p & 1));
@@ -655,8 +679,8 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
         uint32_t ml = par ? xb : xa, mr = par ? xa : xb;
         ml = xsa(ml, __shfl_xor_sync(0xFFFFFFFFu, ml, 4)) & 0x7FFF7FFFu;
         mr = xsa(mr, __shfl_xor_sync(0xFFFFFFFFu, mr, 4)) & 0x7FFF7FFFu;
-        const uint32_t sl0 = block_scale(bf16_lo(ml), g), sl1 = block_scale(bf16_hi(ml), g);
-        const uint32_t sr0 = block_scale(bf16_lo(mr), g), sr1 = block_scale(bf16_hi(mr), g);
+        const uint32_t sl = block_scale2(bf16_lo(ml), bf16_hi(ml), g), sr = block_scale2(bf16_lo(mr), bf16_hi(mr), g);
+        const uint32_t sl0 = sl & 0xFFu, sl1 = sl >> 8, sr0 = sr & 0xFFu, sr1 = sr >> 8;  // columns 2p, 2p + 1
         const float fl0 = rtab[sl0], fl1 = rtab[sl1], fr0 = rtab[sr0], fr1 = rtab[sr1];
         const uint32_t wa0 = encode_half_col(s.a, 2 * p, par ? fr0 : fl0);
         const uint32_t wa1 = encode_half_col(s.a, 2 * p + 1, par ? fr1 : fl1);
@@ -666,8 +690,8 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
         put_col(2 * p + 1, par ? wb1 : wa1);
         put_col(8 + 2 * p, par ? wa0 : wb0);
         put_col(8 + 2 * p + 1, par ? wa1 : wb1);
-        pl[p >> 1] |= (sl0 | (sl1 << 8)) << (16 * (p & 1));
-        pr[p >> 1] |= (sr0 | (sr1 << 8)) << (16 * (p & 1));
+        pl[p >> 1] |= sl << (16 * (p & 1));
+        pr[p >> 1] |= sr << (16 * (p & 1));
       }
       col_pl[0] = pl[0]; col_pl[1] = pl[1]; col_pr[0] = pr[0]; col_pr[1] = pr[1];
       if (!kRow) {
@@ -685,11 +709,11 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const uint32_t pr = row_pair_max_w(s, 2 * t, 2 * t + 1);
-        const uint32_t s0 = block_scale(bf16_lo(pr), g), s1 = block_scale(bf16_hi(pr), g);
+        const uint32_t s01 = block_scale2(bf16_lo(pr), bf16_hi(pr), g), s0 = s01 & 0xFFu, s1 = s01 >> 8;
         const float f0 = rtab[s0], f1 = rtab[s1];
         put_row(2 * t, encode_half_row(s.a[2 * t], f0), encode_half_row(s.b[2 * t], f0));
         put_row(2 * t + 1, encode_half_row(s.a[2 * t + 1], f1), encode_half_row(s.b[2 * t + 1], f1));
-        packed[t >> 1] |= (s0 | (s1 << 8)) << (16 * (t & 1));
+        packed[t >> 1] |= s01 << (16 * (t & 1));
       }
       hooks.data_done(packed[0] ^ packed[1]);  // scales of every row
       hooks.scale_wait();
