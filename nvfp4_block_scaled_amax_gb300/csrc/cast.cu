@@ -42,7 +42,17 @@ struct Smem {
   uint8_t* sc_col;  // [2][kScRegion] staged column-wise scales
   uint64_t* bars;   // [kStages]
   int* abort_flag;
+  // Hadamard column transform (BF16): operand B, its MMA barrier and the
+  // tensor-memory address live in the unused tails of the staging regions
+  // (a row-wise region uses bytes 0..7 * kScPitchRow + 127, a column-wise
+  // one 0..7 * kScPitchCol + 127), so the cast keeps two CTAs per SM.
+  uint8_t* hmat;    // n-group g (8 columns of B, 256 bytes) at hmat + g * kScRegion
+  uint64_t* mma_bar;
+  uint32_t* tmem_slot;
 };
+constexpr int kHmatOffset = 1280, kMmaBarOffset = 1472;
+static_assert(7 * kScPitchRow + 128 <= kHmatOffset && kHmatOffset + 256 <= kScRegion, "row staging tail");
+static_assert(7 * kScPitchCol + 128 <= kMmaBarOffset && kMmaBarOffset + 12 <= kScRegion, "column staging tail");
 
 template <typename T>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
@@ -58,80 +68,85 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.sc_col = s.sc_row + 2 * kScRegion;
   s.bars = reinterpret_cast<uint64_t*>(s.sc_col + 2 * kScRegion);
   s.abort_flag = reinterpret_cast<int*>(s.bars + TileCfg<T>::kStages);
+  s.hmat = s.sc_row + kHmatOffset;
+  s.mma_bar = reinterpret_cast<uint64_t*>(s.sc_col + kMmaBarOffset);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.sc_col + kMmaBarOffset + 8);
   return s;
 }
 
 // ---------------------------------------------------------------------------
-// Hadamard column pass (BF16): warp w -> box w % 2, rows 64 ((w / 2) % 2) ..
-// +64, box columns 32 (w / 4) .. +32; lane l -> columns 2 (l % 16), +1 of
-// those and rows 32 (l / 16) .. +32 of those.  Each column is two 16-row
-// blocks per lane, each transformed as (1/4) H16 diag(sign) v and rounded to
-// BF16 before its amax, scale and codes.  Lanes l and l + 16 hold the two
-// halves of 64 rows of a column: one 16-byte store each, together a whole
-// 32-byte sector of the column-wise output.
+// Hadamard column pass (BF16) on the tensor cores.  For each 16-row block kk
+// of the staged tile, D_kk (128 x 16, FP32, tensor memory) = A_kk * B with
+// A_kk[m][k] = x[16 kk + k][m] read straight from the TMA tile (MN-major,
+// 128-byte swizzle: the two 64-column boxes are the M halves, 8-row groups
+// 1024 bytes apart) and B[k][n] = sign_k H16[n][k] / 4 (exact in BF16), so
+// that D_kk[m][n] is output n of the transform of column m's block.  Every
+// product is exact and the sums are FP32 (their order is the tensor core's;
+// codes may then differ from a left-to-right sum at rounding ties only).
+// Thread (warp w, lane l) then owns column m = 32 (w % 4) + l (tensor-memory
+// lane m) and blocks kk = 4 (w / 4) .. +3: rounds each output to BF16, takes
+// the block maximum, scale and codes, and writes the column's 64 rows as one
+// 32-byte run of the column-wise output.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void rht_col_pass(const uint8_t* st, const Smem& sm, const CastArgs& a, int64_t r0,
-                                             int64_t c0, float g_col, const float* sgn, int parity) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int box = warp & 1, li = lane & 15;
-  const int rbase = ((warp >> 1) & 1) * 64 + (lane >> 4) * 32;
-  const int cbox = (warp >> 2) * 32 + 2 * li;  // first of the lane's two columns within the box
-  uint32_t w[32];
-#pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const int row = rbase + r;
-    w[r] = *reinterpret_cast<const uint32_t*>(st + swz(box, row, cbox >> 3) + ((cbox & 7) << 1));
+// B as 8x8 core matrices (K-major, no swizzle): element (k, n) at
+// (n / 8) * kScRegion + (k / 8) * 128 + (n % 8) * 16 + (k % 8) * 2.
+__device__ __forceinline__ void fill_hadamard_operand(uint8_t* hmat, uint32_t sign_mask) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    const int k = i >> 4, n = i & 15;
+    const bool neg = (((sign_mask >> k) & 1u) != 0) != ((__popc(n & k) & 1) != 0);
+    const uint16_t v = neg ? 0xBE80u : 0x3E80u;  // -0.25 / +0.25 in BF16
+    *reinterpret_cast<uint16_t*>(hmat + (n >> 3) * kScRegion + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) = v;
   }
-  const int64_t rg = r0 + rbase;
-  // The lane's two columns travel together as FP32x2 pairs (column cbox in
-  // the low half): packed sign products and butterflies, one BF16x2
-  // rounding per row, packed block maxima; each column keeps its own scale.
-  uint32_t code[2][4];  // [column][16-row block pair of words]
+}
+
+// One thread: the eight block transforms of the staged tile at `st`.
+__device__ __forceinline__ void rht_issue_mma(const uint8_t* st, const Smem& sm, uint32_t tmem) {
+  constexpr uint32_t kIdesc = umma_idesc_bf16(128, 16, true);
+  const uint64_t bdesc = umma_smem_desc(smem_u32(sm.hmat), 128, kScRegion, 0);
+  tcgen05_after_sync();
 #pragma unroll
-  for (int blk = 0; blk < 2; ++blk) {
-    uint64_t v[16];
+  for (int kk = 0; kk < 8; ++kk)
+    umma_bf16(tmem + 16 * kk, umma_smem_desc(smem_u32(st) + kk * 16 * 128, kBoxBytes, 1024, 2), bdesc, kIdesc, 0);
+  umma_commit(sm.mma_bar);
+}
+
+__device__ __forceinline__ void rht_col_epilogue(uint32_t tmem, const Smem& sm, const CastArgs& a, int64_t r0,
+                                                 int64_t c0, float g_col, int parity) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3, half = warp >> 2;
+  const int m = 32 * q + lane;  // tile column
+  uint32_t code[8];             // rows 64 half .. +64 of column m, eight per word
 #pragma unroll
-    for (int r = 0; r < 16; ++r) v[r] = bf16x2_scaled(w[16 * blk + r], sgn[r]);
-    fwht16_x2(v);
-    uint32_t hb[16];  // BF16x2 of the transformed row: column cbox low, cbox + 1 high
-    uint32_t acc = 0;
+  for (int j = 0; j < 4; ++j) {
+    const int kk = 4 * half + j;
+    uint32_t v[16];
+    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * kk, v);
+    uint32_t hb[8], acc = 0;  // BF16 pairs: rows 2i (low) and 2i + 1
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      hb[r] = pair_to_bf16x2(v[r]);
-      acc = xsa(acc, hb[r]);
+    for (int i = 0; i < 8; ++i) {
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hb[i]) : "f"(__uint_as_float(v[2 * i + 1])), "f"(__uint_as_float(v[2 * i])));
+      acc = xsa(acc, hb[i]);
     }
     acc &= 0x7FFF7FFFu;
-    const uint32_t s01 = block_scale2(bf16_lo(acc), bf16_hi(acc), g_col), s0 = s01 & 0xFFu, s1 = s01 >> 8;
-    const uint64_t rr = mul2(sm.rtab_col[s0], sm.rtab_col[s1], splat2(1.0f));
-    float p[16][2];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const uint64_t pr = mul2(bf16_lo(hb[r]), bf16_hi(hb[r]), rr);
-      asm("mov.b64 {%0, %1}, %2;" : "=f"(p[r][0]), "=f"(p[r][1]) : "l"(pr));
-    }
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      code[cc][2 * blk] = e2m1x8(p[0][cc], p[1][cc], p[2][cc], p[3][cc], p[4][cc], p[5][cc], p[6][cc], p[7][cc]);
-      code[cc][2 * blk + 1] =
-          e2m1x8(p[8][cc], p[9][cc], p[10][cc], p[11][cc], p[12][cc], p[13][cc], p[14][cc], p[15][cc]);
-    }
-    const int tcol = box * 64 + cbox;
-    sm.sc_col[parity * kScRegion + ((rbase >> 4) + blk) * kScPitchCol + tcol] = (uint8_t)s0;
-    sm.sc_col[parity * kScRegion + ((rbase >> 4) + blk) * kScPitchCol + tcol + 1] = (uint8_t)s1;
+    const uint32_t s = block_scale(fmaxf(bf16_lo(acc), bf16_hi(acc)), g_col);
+    const float r = sm.rtab_col[s];
+    code[2 * j] = encode8(bf16_lo(hb[0]), bf16_hi(hb[0]), bf16_lo(hb[1]), bf16_hi(hb[1]), bf16_lo(hb[2]),
+                          bf16_hi(hb[2]), bf16_lo(hb[3]), bf16_hi(hb[3]), r);
+    code[2 * j + 1] = encode8(bf16_lo(hb[4]), bf16_hi(hb[4]), bf16_lo(hb[5]), bf16_hi(hb[5]), bf16_lo(hb[6]),
+                              bf16_hi(hb[6]), bf16_lo(hb[7]), bf16_hi(hb[7]), r);
+    sm.sc_col[parity * kScRegion + kk * kScPitchCol + m] = (uint8_t)s;
   }
+  const int64_t x = c0 + m, rg = r0 + 64 * half;
+  // M % 16 == 0: block kk is inside x when its first row is.
+  if (x < a.N && rg < a.M) {
+    uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
+    if (rg + 64 <= a.M && ((a.M / 2) & 15) == 0) {
+      st_cs_v4(dst, code[0], code[1], code[2], code[3]);
+      st_cs_v4(dst + 16, code[4], code[5], code[6], code[7]);
+    } else {
 #pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
-    const int64_t x = c0 + box * 64 + cbox + cc;
-    // M % 16 == 0: the first block is inside when rg < M, the second when
-    // rg + 16 < M.
-    if (x < a.N && rg < a.M) {
-      uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
-      if (rg + 32 <= a.M && ((a.M / 2) & 15) == 0) {
-        st_cs_v4(dst, code[cc][0], code[cc][1], code[cc][2], code[cc][3]);
-      } else {
-        st_cs_v2(dst, code[cc][0], code[cc][1]);
-        if (rg + 16 < a.M) st_cs_v2(dst + 8, code[cc][2], code[cc][3]);
-      }
+      for (int j = 0; j < 4; ++j)
+        if (rg + 16 * j < a.M) st_cs_v2(dst + 8 * j, code[2 * j], code[2 * j + 1]);
     }
   }
 }
@@ -180,10 +195,26 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
     sm.rtab_row[tid] = encode_factor((uint32_t)tid, g_row);
   else
     sm.rtab_col[tid - 128] = encode_factor((uint32_t)(tid - 128), g_col);
-  float sgn[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) sgn[i] = ((a.sign_mask >> i) & 1u) ? -0.25f : 0.25f;
+  // Hadamard column pass: the operand, the MMA barrier and 128 tensor-memory
+  // columns (one tile's eight 128 x 16 FP32 results; two CTAs per SM use 256
+  // of the 512).
+  const bool tc_cols = MODE == kCastRHT && a.colwise != 0;
+  uint32_t tmem = 0;
+  if (tc_cols) {
+    fill_hadamard_operand(sm.hmat, a.sign_mask);
+    fence_proxy_async_shared();  // the operand, before the tensor cores read it
+    if (tid == 0) {
+      mbar_init(sm.mma_bar, 1);
+      fence_mbar_init();
+    }
+    if ((tid >> 5) == 0) tmem_alloc(sm.tmem_slot, 128);
+    tcgen05_before_sync();
+  }
   __syncthreads();
+  if (tc_cols) {
+    tcgen05_after_sync();
+    tmem = *reinterpret_cast<volatile uint32_t*>(sm.tmem_slot);
+  }
 
   const bool do_row = a.rowwise != 0;
   const bool do_col_blk = a.colwise != 0 && MODE != kCastRHT;
@@ -199,12 +230,25 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
     const int64_t r0 = (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
     const uint8_t* st = sm.stages + (size_t)s * tile_bytes<T>();
     const int parity = k & 1;
+    if constexpr (MODE == kCastRHT) {
+      if (ok && tc_cols && tid == 0) rht_issue_mma(st, sm, tmem);  // runs beside the row-wise pass
+    }
     if (ok && (do_row || do_col_blk))
       block_pass_any<T, MODE>(smem_u32(st), sm.rtab_row, sm.rtab_col, smem_u32(sm.sc_row + parity * kScRegion),
                               smem_u32(sm.sc_col + parity * kScRegion), a, r0, c0, g_row, g_col, do_row, do_col_blk,
                               threadIdx.x >> 5);
     if constexpr (MODE == kCastRHT) {
-      if (ok && a.colwise) rht_col_pass(st, sm, a, r0, c0, g_col, sgn, parity);
+      if (ok && tc_cols) {
+        // the transforms of tile k complete (k-th phase of the MMA barrier)
+        const bool done = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(sm.mma_bar, (uint32_t)(k & 1), a.status));
+        if (done) {
+          tcgen05_after_sync();
+          rht_col_epilogue(tmem, sm, a, r0, c0, g_col, parity);
+        } else {
+          *sm.abort_flag = 1;
+        }
+        tcgen05_before_sync();
+      }
     }
     __syncthreads();  // stage s fully read; this tile's scales staged
     if (*sm.abort_flag) break;
@@ -212,12 +256,16 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
     // this tile's scales: threads 0..127 row-wise, 128..255 column-wise
     if (tid < 128) {
       if (do_row)
-        store_scale_tile<MODE, false>(smem_u32(sm.sc_row + parity * kScRegion), a.scale_row, r0, c0 / 16, a.M,
-                                      a.N / 16, a.swizzled, tid);
+        store_scale_tile<MODE, false>(sm.sc_row + parity * kScRegion, a.scale_row, r0, c0 / 16, a.M, a.N / 16,
+                                      a.swizzled, tid);
     } else if (a.colwise) {
-      store_scale_tile<MODE, true>(smem_u32(sm.sc_col + parity * kScRegion), a.scale_col, c0, r0 / 16, a.N,
-                                   a.M / 16, a.swizzled, tid - 128);
+      store_scale_tile<MODE, true>(sm.sc_col + parity * kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16,
+                                   a.swizzled, tid - 128);
     }
+  }
+  if (tc_cols && (tid >> 5) == 0) {
+    tcgen05_after_sync();
+    tmem_dealloc(tmem, 128);
   }
   if (k < my_count && tid == 0) {
     // A wait ran out: wait (bounded) for this CTA's copies still in flight

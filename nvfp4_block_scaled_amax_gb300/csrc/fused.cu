@@ -421,8 +421,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // have staged them), and a buffer is reused only after every warp's share
   // of its previous contents has been written back.
   const bool do_row = a.rowwise != 0, do_col = a.colwise != 0;
-  // BF16, 128x4 layout (M, N multiples of 128): scales leave by bulk copies
-  const bool bulk = sizeof(T) == 2 && a.swizzled != 0;
   const int k_top = n - 1 - ((n - 1 - grp) % kGroups + kGroups) % kGroups;  // largest k < n, k == grp mod kGroups
   const volatile int* abort_flag = sm.abort_flag;
   auto buffer = [&](int it) { return sm.sc + (size_t)((grp * 2 + (it & 1)) * 2) * kScRegion; };
@@ -436,28 +434,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int per = a.swizzled ? 64 / WPT : 128 / WPT;  // 16-byte lines or rows per warp
     if (lane < per) {
       const int t = cw * per + lane;
-      if (do_row) store_scale_tile<MODE, false>(smem_u32(sc), a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
+      if (do_row) store_scale_tile<MODE, false>(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
       if (do_col)
-        store_scale_tile<MODE, true>(smem_u32(sc + kScRegion), a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled,
-                                     t);
+        store_scale_tile<MODE, true>(sc + kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
     }
     __syncwarp();  // the lanes' reads of the buffer are complete (their stores used them)
     if (lane == 0) atomicAdd(&sm.wb[q], 1u);
     return true;
   };
   int it = 0, k_prev = -1;
-  int pending_q = -1;  // lane 0, bulk mode: buffer of the copies this warp issued, not yet freed
-  auto free_pending = [&] {
-    if (lane == 0 && pending_q >= 0) {
-      bulk_wait_read_all();
-      __threadfence_block();
-      atomicAdd(&sm.wb[pending_q], (unsigned)WPT);
-      pending_q = -1;
-    }
-  };
   for (int k = k_top; k >= 0; k -= kGroups, ++it) {
     const int s = k % S;
-    free_pending();
     if (*abort_flag) break;
     if (k < kept_from && !wait_full(k)) {  // a wait ran out: outputs unfinished
       *sm.abort_flag = 1;
@@ -475,7 +462,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const auto hooks = make_hooks([&](uint32_t token) { release_data(s, k - S, stream, token); }, scale_wait,
                                     use_pre ? sm.pre + k * 64 : nullptr);
       wide_pass_any<MODE>(st, sm.rtab_row, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, do_row, do_col, cw,
-                          bulk, hooks);
+                          hooks);
     } else {
       scale_wait();
       block_pass_any<T, MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g,
@@ -488,42 +475,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       *sm.abort_flag = 1;
       break;
     }
-    if (bulk) {
-      // The group's last warp to finish staging writes the tile's scales
-      // with one bulk copy per direction (staged in the stored byte order);
-      // the buffer is freed once the copies have read it.
-      fence_proxy_async_shared();  // this lane's staging stores, before the copy engine reads them
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        const int q = grp * 2 + (it & 1);
-        if (atomicAdd(&sm.staged[q], 1u) % WPT == (unsigned)(WPT - 1)) {
-          __threadfence_block();
-          if (do_row)
-            bulk_store(a.scale_row + ((r0 >> 7) * (a.N >> 6) + (c0 >> 6)) * 512, smem_u32(sc), 1024);
-          if (do_col)
-            bulk_store(a.scale_col + ((c0 >> 7) * (a.M >> 6) + (r0 >> 6)) * 512, smem_u32(sc + kScRegion), 1024);
-          bulk_commit();
-          pending_q = q;  // freed at this warp's next iteration, when the copies have long read it
-        }
-      }
-      __syncwarp();
-    } else {
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();  // this warp's staged scales before its count
-        atomicAdd(&sm.staged[grp * 2 + (it & 1)], 1u);
-      }
-      if (k_prev >= 0 && !write_back_share(k_prev, it - 1)) {
-        *sm.abort_flag = 1;
-        break;
-      }
-      k_prev = k;
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();  // this warp's staged scales before its count
+      atomicAdd(&sm.staged[grp * 2 + (it & 1)], 1u);
     }
+    if (k_prev >= 0 && !write_back_share(k_prev, it - 1)) {
+      *sm.abort_flag = 1;
+      break;
+    }
+    k_prev = k;
   }
   if (k_prev >= 0 && !*abort_flag && !write_back_share(k_prev, it - 1)) *sm.abort_flag = 1;
-  free_pending();
-  if (lane == 0) bulk_wait_all();  // this warp's scale copies (if any) are complete
   // After an abort, the last warp to leave lets the copies still in flight
   // (the latest load into each stage) land, bounded, before the CTA exits.
   __syncwarp();

@@ -147,7 +147,11 @@ nvfp4_status quantize_per_tensor(int mode, const void* x, int dtype, int64_t M, 
   a.colwise = col;
   a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
   a.sign_mask = sign_mask & 0xFFFFu;
-  return from_cuda(launch_cast(x, bf16, mode, a, /*pdl=*/!skip, ctx));
+  // Without the column-wise output the transform plays no part: the row-wise
+  // output is the 1D cast of x (amax max|x|), by the kernel that has no
+  // tensor-core column pass.
+  const int cast_mode = (mode == kCastRHT && !col) ? kCast1D : mode;
+  return from_cuda(launch_cast(x, bf16, cast_mode, a, /*pdl=*/!skip, ctx));
 }
 
 nvfp4_status quantize_single_pass(int mode, const void* x, int dtype, int64_t M, int64_t N,

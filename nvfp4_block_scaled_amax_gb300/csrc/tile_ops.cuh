@@ -52,31 +52,12 @@ __host__ __device__ constexpr int tile_bytes() {
 constexpr int kScPitchRow = 160, kScPitchCol = 192;
 constexpr int kScRegion = 8 * kScPitchCol;  // bytes per direction
 
-// Explicit shared-memory loads of staged scales (a generic load could alias
-// global memory, so it would be ordered behind the warp's pending stores).
-// The "memory" clobber keeps them after the waits that publish the scales.
-__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-  return v;
-}
-
 template <int MODE, bool kColDir>
-__device__ __forceinline__ uint32_t staged_scale(uint32_t s, int r, int c) {
+__device__ __forceinline__ uint32_t staged_scale(const uint8_t* s, int r, int c) {
   if constexpr (MODE == kCast2D)
-    return lds_u8(s + (uint32_t)((r >> 4) * 8 + c));
+    return s[(r >> 4) * 8 + c];
   else
-    return lds_u8(s + (uint32_t)(c * (kColDir ? kScPitchCol : kScPitchRow) + r));
+    return s[c * (kColDir ? kScPitchCol : kScPitchRow) + r];
 }
 
 // stages | 2 encode-factor tables | 2 x 2 staged scale regions | barriers | flag
@@ -535,14 +516,6 @@ __device__ __forceinline__ float wide_tile_max(const uint32_t (&a)[8][4], const 
   return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
 }
 
-// Byte offset, in a tile's staged atoms of the 128x4 layout, of the word of
-// scale row `r` (0..127: a tile row for row-wise scales, a tile column for
-// column-wise ones) in atom `h` (0, 1: column blocks 4h..4h+3 of that row):
-// 16-byte line r & 31, word r >> 5.
-__device__ __forceinline__ uint32_t stage_swz_offset(int r, int h) {
-  return (uint32_t)(h * 512 + (r & 31) * 16 + (r >> 5) * 4);
-}
-
 // Casts this lane's 8x16 sub-tile (wide mapping) of the staged tile at shared
 // address `stage`: stores its codes and stages its scales (staged_scale
 // layouts) at sc_row / sc_col.  `warp` is the warp's index (0..3) among the
@@ -556,10 +529,7 @@ __device__ __forceinline__ uint32_t stage_swz_offset(int r, int h) {
 // hooks.scale_wait() before its first write to sc_row / sc_col.  In 2D,
 // hooks.tile_max() may give the tile's 16x16 maxima (BF16 bits, [ty][tx])
 // found while the tile was first read; else they are computed here.
-// kSwz (tiles inside x, 128x4 layout): the scales are staged as the tile's
-// two 512-byte atoms per direction, byte for byte as they are stored (see
-// stage_swz_offset), so that one bulk copy per direction writes them.
-template <int MODE, int kDirs, bool kInterior, bool kSwz = false, class Hooks = NoHooks>
+template <int MODE, int kDirs, bool kInterior, class Hooks = NoHooks>
 __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uint32_t sc_row, uint32_t sc_col,
                                           const CastArgs& a, int64_t r0, int64_t c0, float g, int warp,
                                           const Hooks& hooks = Hooks()) {
@@ -628,26 +598,10 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
         put_col(8 + c, par ? ca[c] : cb[c]);
       }
     }
-    if constexpr (kSwz) {
-      // the four column blocks of a row (lanes j) and the four row blocks of
-      // a column (lanes i >> 1) gathered into the 4-byte word they share
-      uint32_t wrow = sb << (8 * j), wcol = sb << (8 * (i >> 1));
-      wrow |= __shfl_xor_sync(0xFFFFFFFFu, wrow, 1);
-      wrow |= __shfl_xor_sync(0xFFFFFFFFu, wrow, 2);
-      wcol |= __shfl_xor_sync(0xFFFFFFFFu, wcol, 8);
-      wcol |= __shfl_xor_sync(0xFFFFFFFFu, wcol, 16);
-      hooks.scale_wait();
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {  // rows trow + 2j + t; columns tcol + 2i + t
-        if (kRow) sts_u32(sc_row + stage_swz_offset(trow + 2 * j + t, tcol >> 6), wrow);
-        if (kCol) sts_u32(sc_col + stage_swz_offset(tcol + 2 * i + t, trow >> 6), wcol);
-      }
-    } else {
-      hooks.scale_wait();
-      if (par == 0) {
-        if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sb);
-        if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sb);
-      }
+    hooks.scale_wait();
+    if (par == 0) {
+      if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sb);
+      if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sb);
     }
   } else {
     // column pass first, then the row pass: only the data stay live between
@@ -659,15 +613,7 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
     // lanes l and l ^ 4 hold the same column-block scales: the lanes with
     // par == 0 stage them (byte c of left / right: column tcol + c / + 8 + c)
     auto stage_col = [&] {
-      if constexpr (kSwz) {
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const uint32_t w = (cc < 8 ? col_pl : col_pr)[(cc & 7) >> 2];
-          sts_u8(sc_col + stage_swz_offset(tcol + cc, trow >> 6) + ((trow >> 4) & 3), w >> (8 * (cc & 3)));
-        }
-      } else {
-        sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), col_pl[0], col_pl[1], col_pr[0], col_pr[1]);
-      }
+      sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), col_pl[0], col_pl[1], col_pr[0], col_pr[1]);
     };
     if (kCol) {
       // column blocks span lanes l and l ^ 4, whose halves A are the other
@@ -718,32 +664,16 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
       hooks.data_done(packed[0] ^ packed[1]);  // scales of every row
       hooks.scale_wait();
       if (kCol && par == 0) stage_col();
-      if constexpr (kSwz) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          sts_u8(sc_row + stage_swz_offset(trow + k, tcol >> 6) + j, packed[k >> 2] >> (8 * (k & 3)));
-      } else {
-        sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
-      }
+      sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
     }
   }
 }
 
-// wide_pass for the directions and tile position at hand; `swz_stage`
-// (tiles inside x): stage the scales in the 128x4 layout's byte order.
+// wide_pass for the directions and tile position at hand.
 template <int MODE, class Hooks = NoHooks>
 __device__ __forceinline__ void wide_pass_any(uint32_t stage, const float* rtab, uint32_t sc_row, uint32_t sc_col,
                                               const CastArgs& a, int64_t r0, int64_t c0, float g, bool do_row,
-                                              bool do_col, int warp, bool swz_stage, const Hooks& h = Hooks()) {
-  if (swz_stage) {
-    if (do_row && do_col)
-      wide_pass<MODE, 3, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
-    else if (do_row)
-      wide_pass<MODE, 1, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
-    else if (do_col)
-      wide_pass<MODE, 2, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
-    return;
-  }
+                                              bool do_col, int warp, const Hooks& h = Hooks()) {
   const bool interior = (r0 + kTile <= a.M) && (c0 + kTile <= a.N);
   if (do_row && do_col) {
     if (interior)
@@ -767,7 +697,7 @@ __device__ __forceinline__ void wide_pass_any(uint32_t stage, const float* rtab,
 // for tile rows R0 .. R0 + 127 and scale columns C0 .. C0 + 7 of an R x C
 // scale matrix; t = 0..127.
 template <int MODE, bool kColDir>
-__device__ __forceinline__ void store_scale_tile(uint32_t s, uint8_t* out, int64_t R0, int64_t C0, int64_t R,
+__device__ __forceinline__ void store_scale_tile(const uint8_t* s, uint8_t* out, int64_t R0, int64_t C0, int64_t R,
                                                  int64_t C, bool swizzled, int t) {
   if (swizzled) {
     // Two 512-byte tiles of the 128x4 layout, contiguous (R, C aligned):
@@ -779,7 +709,7 @@ __device__ __forceinline__ void store_scale_tile(uint32_t s, uint8_t* out, int64
     for (int qq = 0; qq < 4; ++qq) {
       const int r = 32 * qq + L;
       if constexpr (MODE == kCast2D) {
-        w[qq] = lds_u32(s + (uint32_t)((r >> 4) * 8 + 4 * h));
+        w[qq] = *reinterpret_cast<const uint32_t*>(s + (r >> 4) * 8 + 4 * h);
       } else {
         w[qq] = staged_scale<MODE, kColDir>(s, r, 4 * h) | (staged_scale<MODE, kColDir>(s, r, 4 * h + 1) << 8) |
                 (staged_scale<MODE, kColDir>(s, r, 4 * h + 2) << 16) |
@@ -796,7 +726,7 @@ __device__ __forceinline__ void store_scale_tile(uint32_t s, uint8_t* out, int64
     uint8_t* p = out + r * C + C0;
     uint32_t v[2];
     if constexpr (MODE == kCast2D) {
-      const uint2 u = lds_v2(s + (uint32_t)((t >> 4) * 8));
+      const uint2 u = *reinterpret_cast<const uint2*>(s + (t >> 4) * 8);
       v[0] = u.x;
       v[1] = u.y;
     } else {
