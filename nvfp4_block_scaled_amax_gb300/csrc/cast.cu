@@ -83,10 +83,11 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 // that D_kk[m][n] is output n of the transform of column m's block.  Every
 // product is exact and the sums are FP32 (their order is the tensor core's;
 // codes may then differ from a left-to-right sum at rounding ties only).
-// Thread (warp w, lane l) then owns column m = 32 (w % 4) + l (tensor-memory
-// lane m) and blocks kk = 4 (w / 4) .. +3: rounds each output to BF16, takes
-// the block maximum, scale and codes, and writes the column's 64 rows as one
-// 32-byte run of the column-wise output.
+// Warps 4..7 then cast the columns while warps 0..3 cast the rows (wide
+// mapping, whole-sector stores): thread (warp w, lane l) owns column
+// m = 32 (w % 4) + l (tensor-memory lane m) and its eight blocks; it rounds
+// each output to BF16, takes the block maximum, scale and codes, and writes
+// each 64 rows of the column as one 32-byte run of the column-wise output.
 // ---------------------------------------------------------------------------
 // B as 8x8 core matrices (K-major, no swizzle): element (k, n) at
 // (n / 8) * kScRegion + (k / 8) * 128 + (n % 8) * 16 + (k % 8) * 2.
@@ -113,40 +114,43 @@ __device__ __forceinline__ void rht_issue_mma(const uint8_t* st, const Smem& sm,
 __device__ __forceinline__ void rht_col_epilogue(uint32_t tmem, const Smem& sm, const CastArgs& a, int64_t r0,
                                                  int64_t c0, float g_col, int parity) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = warp & 3, half = warp >> 2;
+  const int q = warp & 3;
   const int m = 32 * q + lane;  // tile column
-  uint32_t code[8];             // rows 64 half .. +64 of column m, eight per word
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int kk = 4 * half + j;
-    uint32_t v[16];
-    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * kk, v);
-    uint32_t hb[8], acc = 0;  // BF16 pairs: rows 2i (low) and 2i + 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t code[8];  // rows 64 half .. +64 of column m, eight per word
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hb[i]) : "f"(__uint_as_float(v[2 * i + 1])), "f"(__uint_as_float(v[2 * i])));
-      acc = xsa(acc, hb[i]);
+    for (int j = 0; j < 4; ++j) {
+      const int kk = 4 * half + j;
+      uint32_t v[16];
+      tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * kk, v);
+      uint32_t hb[8], acc = 0;  // BF16 pairs: rows 2i (low) and 2i + 1
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hb[i]) : "f"(__uint_as_float(v[2 * i + 1])), "f"(__uint_as_float(v[2 * i])));
+        acc = xsa(acc, hb[i]);
+      }
+      acc &= 0x7FFF7FFFu;
+      const uint32_t s = block_scale(fmaxf(bf16_lo(acc), bf16_hi(acc)), g_col);
+      const float r = sm.rtab_col[s];
+      code[2 * j] = encode8(bf16_lo(hb[0]), bf16_hi(hb[0]), bf16_lo(hb[1]), bf16_hi(hb[1]), bf16_lo(hb[2]),
+                            bf16_hi(hb[2]), bf16_lo(hb[3]), bf16_hi(hb[3]), r);
+      code[2 * j + 1] = encode8(bf16_lo(hb[4]), bf16_hi(hb[4]), bf16_lo(hb[5]), bf16_hi(hb[5]), bf16_lo(hb[6]),
+                                bf16_hi(hb[6]), bf16_lo(hb[7]), bf16_hi(hb[7]), r);
+      sm.sc_col[parity * kScRegion + kk * kScPitchCol + m] = (uint8_t)s;
     }
-    acc &= 0x7FFF7FFFu;
-    const uint32_t s = block_scale(fmaxf(bf16_lo(acc), bf16_hi(acc)), g_col);
-    const float r = sm.rtab_col[s];
-    code[2 * j] = encode8(bf16_lo(hb[0]), bf16_hi(hb[0]), bf16_lo(hb[1]), bf16_hi(hb[1]), bf16_lo(hb[2]),
-                          bf16_hi(hb[2]), bf16_lo(hb[3]), bf16_hi(hb[3]), r);
-    code[2 * j + 1] = encode8(bf16_lo(hb[4]), bf16_hi(hb[4]), bf16_lo(hb[5]), bf16_hi(hb[5]), bf16_lo(hb[6]),
-                              bf16_hi(hb[6]), bf16_lo(hb[7]), bf16_hi(hb[7]), r);
-    sm.sc_col[parity * kScRegion + kk * kScPitchCol + m] = (uint8_t)s;
-  }
-  const int64_t x = c0 + m, rg = r0 + 64 * half;
-  // M % 16 == 0: block kk is inside x when its first row is.
-  if (x < a.N && rg < a.M) {
-    uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
-    if (rg + 64 <= a.M && ((a.M / 2) & 15) == 0) {
-      st_cs_v4(dst, code[0], code[1], code[2], code[3]);
-      st_cs_v4(dst + 16, code[4], code[5], code[6], code[7]);
-    } else {
+    const int64_t x = c0 + m, rg = r0 + 64 * half;
+    // M % 16 == 0: block kk is inside x when its first row is.
+    if (x < a.N && rg < a.M) {
+      uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
+      if (rg + 64 <= a.M && ((a.M / 2) & 15) == 0) {
+        st_cs_v4(dst, code[0], code[1], code[2], code[3]);
+        st_cs_v4(dst + 16, code[4], code[5], code[6], code[7]);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (rg + 16 * j < a.M) st_cs_v2(dst + 8 * j, code[2 * j], code[2 * j + 1]);
+        for (int j = 0; j < 4; ++j)
+          if (rg + 16 * j < a.M) st_cs_v2(dst + 8 * j, code[2 * j], code[2 * j + 1]);
+      }
     }
   }
 }
@@ -230,26 +234,33 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
     const int64_t r0 = (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
     const uint8_t* st = sm.stages + (size_t)s * tile_bytes<T>();
     const int parity = k & 1;
-    if constexpr (MODE == kCastRHT) {
-      if (ok && tc_cols && tid == 0) rht_issue_mma(st, sm, tmem);  // runs beside the row-wise pass
-    }
-    if (ok && (do_row || do_col_blk))
-      block_pass_any<T, MODE>(smem_u32(st), sm.rtab_row, sm.rtab_col, smem_u32(sm.sc_row + parity * kScRegion),
-                              smem_u32(sm.sc_col + parity * kScRegion), a, r0, c0, g_row, g_col, do_row, do_col_blk,
-                              threadIdx.x >> 5);
-    if constexpr (MODE == kCastRHT) {
-      if (ok && tc_cols) {
-        // the transforms of tile k complete (k-th phase of the MMA barrier)
-        const bool done = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(sm.mma_bar, (uint32_t)(k & 1), a.status));
-        if (done) {
-          tcgen05_after_sync();
-          rht_col_epilogue(tmem, sm, a, r0, c0, g_col, parity);
-        } else {
-          *sm.abort_flag = 1;
+    bool tc_done = false;
+    if constexpr (MODE == kCastRHT && sizeof(T) == 2) {
+      if (tc_cols) {
+        tc_done = true;
+        const int warp = tid >> 5;
+        if (ok && tid == 0) rht_issue_mma(st, sm, tmem);
+        if (ok && warp < 4) {
+          if (do_row)
+            wide_pass_any<kCast1D>(smem_u32(st), sm.rtab_row, smem_u32(sm.sc_row + parity * kScRegion),
+                                   smem_u32(sm.sc_col + parity * kScRegion), a, r0, c0, g_row, true, false, warp);
+        } else if (ok) {
+          // the transforms of tile k complete (k-th phase of the MMA barrier)
+          const bool done = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(sm.mma_bar, (uint32_t)(k & 1), a.status));
+          if (done) {
+            tcgen05_after_sync();
+            rht_col_epilogue(tmem, sm, a, r0, c0, g_col, parity);
+          } else {
+            *sm.abort_flag = 1;
+          }
         }
         tcgen05_before_sync();
       }
     }
+    if (ok && !tc_done && (do_row || do_col_blk))
+      block_pass_any<T, MODE>(smem_u32(st), sm.rtab_row, sm.rtab_col, smem_u32(sm.sc_row + parity * kScRegion),
+                              smem_u32(sm.sc_col + parity * kScRegion), a, r0, c0, g_row, g_col, do_row, do_col_blk,
+                              threadIdx.x >> 5);
     __syncthreads();  // stage s fully read; this tile's scales staged
     if (*sm.abort_flag) break;
     if (tid == 0 && k + C::kStages < my_count) issue(k + C::kStages);
