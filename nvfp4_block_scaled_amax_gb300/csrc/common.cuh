@@ -244,6 +244,22 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Bulk (non-tensor) copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from shared to global memory, in this thread's bulk group.  The
+// shared data must have been made visible to the async proxy first
+// (fence_proxy_async_shared by each thread that wrote it, then a hand-over).
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's committed bulk copies have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's committed bulk copies are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Tensor memory and the 5th-generation tensor cores (tcgen05)
 // ---------------------------------------------------------------------------
@@ -321,6 +337,9 @@ __device__ __forceinline__ void st_cs_u32_if(void* p, uint32_t a, uint32_t pred)
   asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q st.global.cs.u32 [%0], %1;\n}" ::"l"(p), "r"(a),
                "r"(pred)
                : "memory");
+}
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void sts_u8(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");

@@ -214,9 +214,13 @@ __device__ __forceinline__ float share_absmax(uint32_t stage, int cw) {
   }
 }
 
-template <typename T, int MODE>
+// kBulk (BF16, 128x4 layout, M and N multiples of 128): the scales are
+// staged in the stored byte order and leave by bulk copies (a separate
+// instantiation, so the compact path carries none of that code).
+template <typename T, int MODE, bool kBulk>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tmap, const CastArgs a, SinglePassWorkspace* ws) {
+  static_assert(!kBulk || sizeof(T) == 2, "bulk scale copies: BF16 wide mapping only");
   constexpr int S = FusedCfg<T>::kStages;
   constexpr int WPT = FusedCfg<T>::kWarpsPerTile;
   constexpr int kGroups = kWarps / WPT;
@@ -443,8 +447,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     return true;
   };
   int it = 0, k_prev = -1;
+  int pending_q = -1;  // lane 0, kBulk: buffer of the copies this warp issued, not yet freed
+  auto free_pending = [&] {
+    if (kBulk && lane == 0 && pending_q >= 0) {
+      bulk_wait_read_all();
+      __threadfence_block();
+      atomicAdd(&sm.wb[pending_q], (unsigned)WPT);
+      pending_q = -1;
+    }
+  };
   for (int k = k_top; k >= 0; k -= kGroups, ++it) {
     const int s = k % S;
+    free_pending();
     if (*abort_flag) break;
     if (k < kept_from && !wait_full(k)) {  // a wait ran out: outputs unfinished
       *sm.abort_flag = 1;
@@ -461,8 +475,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if constexpr (sizeof(T) == 2) {
       const auto hooks = make_hooks([&](uint32_t token) { release_data(s, k - S, stream, token); }, scale_wait,
                                     use_pre ? sm.pre + k * 64 : nullptr);
-      wide_pass_any<MODE>(st, sm.rtab_row, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, do_row, do_col, cw,
-                          hooks);
+      wide_pass_any<MODE, kBulk>(st, sm.rtab_row, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, do_row,
+                                 do_col, cw, hooks);
     } else {
       scale_wait();
       block_pass_any<T, MODE>(st, sm.rtab_row, sm.rtab_col, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g,
@@ -475,18 +489,44 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       *sm.abort_flag = 1;
       break;
     }
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence_block();  // this warp's staged scales before its count
-      atomicAdd(&sm.staged[grp * 2 + (it & 1)], 1u);
+    if constexpr (kBulk) {
+      // The group's last warp to finish staging writes the tile's scales
+      // with one bulk copy per direction; the buffer is freed once the
+      // copies have read it (at that warp's next iteration).
+      fence_proxy_async_shared();  // this lane's staging stores, before the copy engine reads them
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        const int q = grp * 2 + (it & 1);
+        if (atomicAdd(&sm.staged[q], 1u) % WPT == (unsigned)(WPT - 1)) {
+          __threadfence_block();
+          if (do_row)
+            bulk_store(a.scale_row + ((r0 >> 7) * (a.N >> 6) + (c0 >> 6)) * 512, smem_u32(sc), 1024);
+          if (do_col)
+            bulk_store(a.scale_col + ((c0 >> 7) * (a.M >> 6) + (r0 >> 6)) * 512, smem_u32(sc + kScRegion), 1024);
+          bulk_commit();
+          pending_q = q;
+        }
+      }
+      __syncwarp();
+    } else {
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();  // this warp's staged scales before its count
+        atomicAdd(&sm.staged[grp * 2 + (it & 1)], 1u);
+      }
+      if (k_prev >= 0 && !write_back_share(k_prev, it - 1)) {
+        *sm.abort_flag = 1;
+        break;
+      }
+      k_prev = k;
     }
-    if (k_prev >= 0 && !write_back_share(k_prev, it - 1)) {
-      *sm.abort_flag = 1;
-      break;
-    }
-    k_prev = k;
   }
   if (k_prev >= 0 && !*abort_flag && !write_back_share(k_prev, it - 1)) *sm.abort_flag = 1;
+  if constexpr (kBulk) {
+    free_pending();
+    if (lane == 0) bulk_wait_all();  // this warp's scale copies (if any) are complete
+  }
   // After an abort, the last warp to leave lets the copies still in flight
   // (the latest load into each stage) land, bounded, before the CTA exits.
   __syncwarp();
@@ -496,9 +536,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
 }
 
-template <typename T, int MODE>
+template <typename T, int MODE, bool kBulk>
 cudaError_t launch_fused_t(const CUtensorMap& map, const CastArgs& a, SinglePassWorkspace* ws, const LaunchCtx& ctx) {
-  auto fn = fused_kernel<T, MODE>;
+  auto fn = fused_kernel<T, MODE, kBulk>;
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -543,11 +583,16 @@ cudaError_t launch_single_pass(const void* x, bool bf16, int mode, CastArgs args
   args.tiles_n = (int)tiles_n;
   args.num_tiles = (int)(tiles_m * tiles_n);
   if (bf16) {
-    if (mode == kCast1D) return launch_fused_t<uint16_t, kCast1D>(map, args, ws, ctx);
-    return launch_fused_t<uint16_t, kCast2D>(map, args, ws, ctx);
+    // the 128x4 layout requires M and N multiples of 128 (validated): every tile is whole
+    if (args.swizzled) {
+      if (mode == kCast1D) return launch_fused_t<uint16_t, kCast1D, true>(map, args, ws, ctx);
+      return launch_fused_t<uint16_t, kCast2D, true>(map, args, ws, ctx);
+    }
+    if (mode == kCast1D) return launch_fused_t<uint16_t, kCast1D, false>(map, args, ws, ctx);
+    return launch_fused_t<uint16_t, kCast2D, false>(map, args, ws, ctx);
   }
-  if (mode == kCast1D) return launch_fused_t<float, kCast1D>(map, args, ws, ctx);
-  return launch_fused_t<float, kCast2D>(map, args, ws, ctx);
+  if (mode == kCast1D) return launch_fused_t<float, kCast1D, false>(map, args, ws, ctx);
+  return launch_fused_t<float, kCast2D, false>(map, args, ws, ctx);
 }
 
 }  // namespace nvfp4

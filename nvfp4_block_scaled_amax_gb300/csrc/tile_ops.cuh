@@ -516,6 +516,14 @@ __device__ __forceinline__ float wide_tile_max(const uint32_t (&a)[8][4], const 
   return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
 }
 
+// Byte offset, in a tile's staged atoms of the 128x4 layout, of the word of
+// scale row `r` (0..127: a tile row for row-wise scales, a tile column for
+// column-wise ones) in atom `h` (0, 1: column blocks 4h..4h+3 of that row):
+// 16-byte line r & 31, word r >> 5.
+__device__ __forceinline__ uint32_t stage_swz_offset(int r, int h) {
+  return (uint32_t)(h * 512 + (r & 31) * 16 + (r >> 5) * 4);
+}
+
 // Casts this lane's 8x16 sub-tile (wide mapping) of the staged tile at shared
 // address `stage`: stores its codes and stages its scales (staged_scale
 // layouts) at sc_row / sc_col.  `warp` is the warp's index (0..3) among the
@@ -529,7 +537,10 @@ __device__ __forceinline__ float wide_tile_max(const uint32_t (&a)[8][4], const 
 // hooks.scale_wait() before its first write to sc_row / sc_col.  In 2D,
 // hooks.tile_max() may give the tile's 16x16 maxima (BF16 bits, [ty][tx])
 // found while the tile was first read; else they are computed here.
-template <int MODE, int kDirs, bool kInterior, class Hooks = NoHooks>
+// kSwz (tiles inside x, 128x4 layout): the scales are staged as the tile's
+// two 512-byte atoms per direction, byte for byte as they are stored (see
+// stage_swz_offset), so that one bulk copy per direction writes them.
+template <int MODE, int kDirs, bool kInterior, bool kSwz = false, class Hooks = NoHooks>
 __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uint32_t sc_row, uint32_t sc_col,
                                           const CastArgs& a, int64_t r0, int64_t c0, float g, int warp,
                                           const Hooks& hooks = Hooks()) {
@@ -598,10 +609,26 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
         put_col(8 + c, par ? ca[c] : cb[c]);
       }
     }
-    hooks.scale_wait();
-    if (par == 0) {
-      if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sb);
-      if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sb);
+    if constexpr (kSwz) {
+      // the four column blocks of a row (lanes j) and the four row blocks of
+      // a column (lanes i >> 1) gathered into the 4-byte word they share
+      uint32_t wrow = sb << (8 * j), wcol = sb << (8 * (i >> 1));
+      wrow |= __shfl_xor_sync(0xFFFFFFFFu, wrow, 1);
+      wrow |= __shfl_xor_sync(0xFFFFFFFFu, wrow, 2);
+      wcol |= __shfl_xor_sync(0xFFFFFFFFu, wcol, 8);
+      wcol |= __shfl_xor_sync(0xFFFFFFFFu, wcol, 16);
+      hooks.scale_wait();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {  // rows trow + 2j + t; columns tcol + 2i + t
+        if (kRow) sts_u32(sc_row + stage_swz_offset(trow + 2 * j + t, tcol >> 6), wrow);
+        if (kCol) sts_u32(sc_col + stage_swz_offset(tcol + 2 * i + t, trow >> 6), wcol);
+      }
+    } else {
+      hooks.scale_wait();
+      if (par == 0) {
+        if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sb);
+        if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sb);
+      }
     }
   } else {
     // column pass first, then the row pass: only the data stay live between
@@ -613,7 +640,15 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
     // lanes l and l ^ 4 hold the same column-block scales: the lanes with
     // par == 0 stage them (byte c of left / right: column tcol + c / + 8 + c)
     auto stage_col = [&] {
-      sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), col_pl[0], col_pl[1], col_pr[0], col_pr[1]);
+      if constexpr (kSwz) {
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const uint32_t w = (cc < 8 ? col_pl : col_pr)[(cc & 7) >> 2];
+          sts_u8(sc_col + stage_swz_offset(tcol + cc, trow >> 6) + ((trow >> 4) & 3), w >> (8 * (cc & 3)));
+        }
+      } else {
+        sts_v4(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), col_pl[0], col_pl[1], col_pr[0], col_pr[1]);
+      }
     };
     if (kCol) {
       // column blocks span lanes l and l ^ 4, whose halves A are the other
@@ -664,16 +699,32 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
       hooks.data_done(packed[0] ^ packed[1]);  // scales of every row
       hooks.scale_wait();
       if (kCol && par == 0) stage_col();
-      sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
+      if constexpr (kSwz) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          sts_u8(sc_row + stage_swz_offset(trow + k, tcol >> 6) + j, packed[k >> 2] >> (8 * (k & 3)));
+      } else {
+        sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
+      }
     }
   }
 }
 
-// wide_pass for the directions and tile position at hand.
-template <int MODE, class Hooks = NoHooks>
+// wide_pass for the directions and tile position at hand; kSwz: scales
+// staged in the 128x4 layout's byte order (every tile inside x).
+template <int MODE, bool kSwz = false, class Hooks = NoHooks>
 __device__ __forceinline__ void wide_pass_any(uint32_t stage, const float* rtab, uint32_t sc_row, uint32_t sc_col,
                                               const CastArgs& a, int64_t r0, int64_t c0, float g, bool do_row,
                                               bool do_col, int warp, const Hooks& h = Hooks()) {
+  if constexpr (kSwz) {
+    if (do_row && do_col)
+      wide_pass<MODE, 3, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
+    else if (do_row)
+      wide_pass<MODE, 1, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
+    else if (do_col)
+      wide_pass<MODE, 2, true, true>(stage, rtab, sc_row, sc_col, a, r0, c0, g, warp, h);
+    return;
+  }
   const bool interior = (r0 + kTile <= a.M) && (c0 + kTile <= a.N);
   if (do_row && do_col) {
     if (interior)
