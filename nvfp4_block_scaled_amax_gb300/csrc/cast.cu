@@ -143,7 +143,9 @@ __device__ __forceinline__ void rht_col_epilogue(uint32_t tmem, const Smem& sm, 
     // M % 16 == 0: block kk is inside x when its first row is.
     if (x < a.N && rg < a.M) {
       uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
-      if (rg + 64 <= a.M && ((a.M / 2) & 15) == 0) {
+      if (rg + 64 <= a.M && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+        st_cs_v8(dst, code);  // the whole 32-byte sector at once
+      } else if (rg + 64 <= a.M && ((a.M / 2) & 15) == 0) {
         st_cs_v4(dst, code[0], code[1], code[2], code[3]);
         st_cs_v4(dst + 16, code[4], code[5], code[6], code[7]);
       } else {
