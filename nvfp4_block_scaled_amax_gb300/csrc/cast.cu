@@ -18,9 +18,9 @@
 //     threads: 16-byte lines of the cuBLAS 128x4 layout ("Fuse NVFP4 scale
 //     swizzling on SM120 and SM121", Changes: aligned groups of four scales
 //     written together), or 8-byte runs of the compact layout.
-// With the random Hadamard transform the column-wise output comes from a
-// second pass over the tile in which each thread owns whole 16-row column
-// blocks (2 columns x 32 rows) and transforms them before the cast.
+// With the random Hadamard transform the column blocks are transformed on
+// the tensor cores (see the Hadamard column pass below) while warps 0-3 cast
+// the rows with the wide mapping of tile_ops.cuh.
 #include <atomic>
 
 #include "common.cuh"
