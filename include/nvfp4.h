@@ -178,7 +178,7 @@ nvfp4_status nvfp4_quantize_rht(const void* x, int dtype, int64_t M, int64_t N,
  *   before its first use and not shared by calls that can run at the same
  *   time; the kernel leaves it ready for the next call (it uses the first 64
  *   bytes: the grid barrier's generation and, for two alternating
- *   generations, an arrival count and a maximum; the rest is reserved).
+ *   generations, an arrival count and two maxima; the rest is reserved).
  *   After a call that reported NVFP4_ERR_TIMEOUT through
  *   nvfp4_device_status, zero it again.
  *   flags: ROWWISE | COLWISE | SWIZZLED (no SKIP_AMAX: use the two-pass
@@ -192,6 +192,22 @@ nvfp4_status nvfp4_quantize_1d_single_pass(const void* x, int dtype, int64_t M, 
 nvfp4_status nvfp4_quantize_2d_single_pass(const void* x, int dtype, int64_t M, int64_t N,
                                            const nvfp4_output* out, unsigned flags, const float* noop,
                                            void* workspace, void* stream);
+/*
+ * Single-launch Hadamard quantize: the results of nvfp4_quantize_rht (within
+ * the same rounding-tie tolerance of the column-wise codes; amax_row =
+ * max|x| and amax_col = max|RHT(x)| exact) from one persistent kernel that
+ * reads x from HBM once: per tile it reduces max|x| and, on the tensor cores,
+ * transforms the tile's 16-row column blocks for max|RHT(x)|; after the grid
+ * barrier it casts the rows of x and transforms the staged or re-read tiles
+ * again for the column-wise cast.  ("Write both NVFP4 amax buffers", review
+ * reply: with RHT the row amax is max|x|, the column amax max|RHT(x)|.)
+ * Workspace, flags and co-residency as above; BF16 input, M % 16 == 0,
+ * N % 16 == 0 (NVFP4_ERR_DTYPE / NVFP4_ERR_SHAPE).  Without COLWISE the
+ * transform plays no part and the call is nvfp4_quantize_1d_single_pass.
+ */
+nvfp4_status nvfp4_quantize_rht_single_pass(const void* x, int dtype, int64_t M, int64_t N,
+                                            const nvfp4_output* out, unsigned flags, uint32_t sign_mask,
+                                            const float* noop, void* workspace, void* stream);
 
 /*
  * nvfp4_quantize_2d_single_pass for callers that cannot allocate device

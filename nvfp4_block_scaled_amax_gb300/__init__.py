@@ -12,11 +12,11 @@ Modes: "1d" (1x16 blocks), "2d" (16x16 tiles), "rht" (random Hadamard
 transform on the column-wise path) and "row_scaled" (one amax per row,
 row-wise only).
 
-Paths for "1d" / "2d": "single_pass" (one persistent kernel: amax, grid
-barrier, cast; x read from HBM once; needs a small workspace, which this
-module keeps per device and stream) and "two_pass" (an amax kernel, then the
-cast kernel; needed for skip_amax).  "auto" picks single_pass when it
-applies.
+Paths for "1d" / "2d" / "rht": "single_pass" (one persistent kernel: amax,
+grid barrier, cast; x read from HBM once; needs a small workspace, which
+this module keeps per device and stream) and "two_pass" (an amax kernel,
+then the cast kernel; needed for skip_amax).  "auto" picks single_pass for
+1d / 2d when it applies and two_pass for rht (measured faster there).
 """
 from __future__ import annotations
 
@@ -200,16 +200,24 @@ def quantize(x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: b
     st = out.c_struct()
     if path not in ("auto", "single_pass", "two_pass"):
         raise ValueError(f"unknown path {path!r}")
-    single = mode in ("1d", "2d") and not skip_amax and path != "two_pass"
+    # rht: the single-pass kernel reads x from HBM once but is not faster than
+    # the two kernels on GB300 (its cast phase is arithmetic-bound), so "auto"
+    # keeps the two-pass path for it
+    single = (mode in ("1d", "2d") or (mode == "rht" and path == "single_pass")) and not skip_amax and \
+        path != "two_pass"
     if path == "single_pass" and not single:
-        raise ValueError("the single-pass path covers 1d / 2d quantize without skip_amax")
+        raise ValueError("the single-pass path covers 1d / 2d / rht quantize without skip_amax")
     with _OnDevice(x.device):
         s = _stream(x.device)
         if single:
             ws = workspace if workspace is not None else single_pass_workspace(x.device, s.value)
             _require_cuda(ws)
-            fn = L.nvfp4_quantize_1d_single_pass if mode == "1d" else L.nvfp4_quantize_2d_single_pass
-            rc = fn(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), _ptr(ws), s)
+            if mode == "rht":
+                rc = L.nvfp4_quantize_rht_single_pass(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags,
+                                                      sign_mask & 0xFFFF, _ptr(noop), _ptr(ws), s)
+            else:
+                fn = L.nvfp4_quantize_1d_single_pass if mode == "1d" else L.nvfp4_quantize_2d_single_pass
+                rc = fn(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), _ptr(ws), s)
         elif mode == "1d":
             rc = L.nvfp4_quantize_1d(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(noop), s)
         elif mode == "2d":

@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_
 # Every symbol the header declares.
 EXPORTS = ("nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_compute_amax", "nvfp4_compute_amax_rht",
            "nvfp4_quantize_1d", "nvfp4_quantize_2d", "nvfp4_quantize_row_scaled", "nvfp4_quantize_rht",
-           "nvfp4_quantize_1d_single_pass", "nvfp4_quantize_2d_single_pass",
+           "nvfp4_quantize_1d_single_pass", "nvfp4_quantize_2d_single_pass", "nvfp4_quantize_rht_single_pass",
            "nvfp4_quantize_2d_single_pass_noalloc",
            "nvfp4_dequantize", "nvfp4_swizzle_scales", "nvfp4_device_status")
 SINGLE_PASS_WORKSPACE_BYTES = 4096
@@ -58,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.nvfp4_quantize_rht.argtypes = [vp, c_int, i64, i64, ctypes.POINTER(Output), uint, u32, vp, vp]
         for name in ("nvfp4_quantize_1d_single_pass", "nvfp4_quantize_2d_single_pass"):
             getattr(L, name).argtypes = [vp, c_int, i64, i64, ctypes.POINTER(Output), uint, vp, vp, vp]
+        L.nvfp4_quantize_rht_single_pass.argtypes = [vp, c_int, i64, i64, ctypes.POINTER(Output), uint, u32, vp, vp,
+                                                     vp]
         L.nvfp4_quantize_2d_single_pass_noalloc.argtypes = [vp, c_int, i64, i64, ctypes.POINTER(Output), uint, vp,
                                                            vp]
         L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, uint, vp, c_int, vp]

@@ -24,6 +24,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "hadamard.cuh"
 #include "kernels.h"
 #include "tile_ops.cuh"
 
@@ -75,87 +76,10 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 }
 
 // ---------------------------------------------------------------------------
-// Hadamard column pass (BF16) on the tensor cores.  For each 16-row block kk
-// of the staged tile, D_kk (128 x 16, FP32, tensor memory) = A_kk * B with
-// A_kk[m][k] = x[16 kk + k][m] read straight from the TMA tile (MN-major,
-// 128-byte swizzle: the two 64-column boxes are the M halves, 8-row groups
-// 1024 bytes apart) and B[k][n] = sign_k H16[n][k] / 4 (exact in BF16), so
-// that D_kk[m][n] is output n of the transform of column m's block.  Every
-// product is exact and the sums are FP32 (their order is the tensor core's;
-// codes may then differ from a left-to-right sum at rounding ties only).
-// Warps 4..7 then cast the columns while warps 0..3 cast the rows (wide
-// mapping, whole-sector stores): thread (warp w, lane l) owns column
-// m = 32 (w % 4) + l (tensor-memory lane m) and its eight blocks; it rounds
-// each output to BF16, takes the block maximum, scale and codes, and writes
-// each 64 rows of the column as one 32-byte run of the column-wise output.
+// Hadamard column pass (BF16): hadamard.cuh.  One thread issues the tile's
+// eight block transforms, which run beside the row-wise pass of warps 0..3;
+// warps 4..7 then cast the columns (warp w owns tile columns 32 (w % 4) ..).
 // ---------------------------------------------------------------------------
-// B as 8x8 core matrices (K-major, no swizzle): element (k, n) at
-// (n / 8) * kScRegion + (k / 8) * 128 + (n % 8) * 16 + (k % 8) * 2.
-__device__ __forceinline__ void fill_hadamard_operand(uint8_t* hmat, uint32_t sign_mask) {
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-    const int k = i >> 4, n = i & 15;
-    const bool neg = (((sign_mask >> k) & 1u) != 0) != ((__popc(n & k) & 1) != 0);
-    const uint16_t v = neg ? 0xBE80u : 0x3E80u;  // -0.25 / +0.25 in BF16
-    *reinterpret_cast<uint16_t*>(hmat + (n >> 3) * kScRegion + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2) = v;
-  }
-}
-
-// One thread: the eight block transforms of the staged tile at `st`.
-__device__ __forceinline__ void rht_issue_mma(const uint8_t* st, const Smem& sm, uint32_t tmem) {
-  constexpr uint32_t kIdesc = umma_idesc_bf16(128, 16, true);
-  const uint64_t bdesc = umma_smem_desc(smem_u32(sm.hmat), 128, kScRegion, 0);
-  tcgen05_after_sync();
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    umma_bf16(tmem + 16 * kk, umma_smem_desc(smem_u32(st) + kk * 16 * 128, kBoxBytes, 1024, 2), bdesc, kIdesc, 0);
-  umma_commit(sm.mma_bar);
-}
-
-__device__ __forceinline__ void rht_col_epilogue(uint32_t tmem, const Smem& sm, const CastArgs& a, int64_t r0,
-                                                 int64_t c0, float g_col, int parity) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = warp & 3;
-  const int m = 32 * q + lane;  // tile column
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t code[8];  // rows 64 half .. +64 of column m, eight per word
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int kk = 4 * half + j;
-      uint32_t v[16];
-      tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * kk, v);
-      uint32_t hb[8], acc = 0;  // BF16 pairs: rows 2i (low) and 2i + 1
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hb[i]) : "f"(__uint_as_float(v[2 * i + 1])), "f"(__uint_as_float(v[2 * i])));
-        acc = xsa(acc, hb[i]);
-      }
-      acc &= 0x7FFF7FFFu;
-      const uint32_t s = block_scale(fmaxf(bf16_lo(acc), bf16_hi(acc)), g_col);
-      const float r = sm.rtab_col[s];
-      code[2 * j] = encode8(bf16_lo(hb[0]), bf16_hi(hb[0]), bf16_lo(hb[1]), bf16_hi(hb[1]), bf16_lo(hb[2]),
-                            bf16_hi(hb[2]), bf16_lo(hb[3]), bf16_hi(hb[3]), r);
-      code[2 * j + 1] = encode8(bf16_lo(hb[4]), bf16_hi(hb[4]), bf16_lo(hb[5]), bf16_hi(hb[5]), bf16_lo(hb[6]),
-                                bf16_hi(hb[6]), bf16_lo(hb[7]), bf16_hi(hb[7]), r);
-      sm.sc_col[parity * kScRegion + kk * kScPitchCol + m] = (uint8_t)s;
-    }
-    const int64_t x = c0 + m, rg = r0 + 64 * half;
-    // M % 16 == 0: block kk is inside x when its first row is.
-    if (x < a.N && rg < a.M) {
-      uint8_t* dst = a.data_col + x * (a.M / 2) + rg / 2;
-      if (rg + 64 <= a.M && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
-        st_cs_v8(dst, code);  // the whole 32-byte sector at once
-      } else if (rg + 64 <= a.M && ((a.M / 2) & 15) == 0) {
-        st_cs_v4(dst, code[0], code[1], code[2], code[3]);
-        st_cs_v4(dst + 16, code[4], code[5], code[6], code[7]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (rg + 16 * j < a.M) st_cs_v2(dst + 8 * j, code[2 * j], code[2 * j + 1]);
-      }
-    }
-  }
-}
 
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
@@ -207,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
   const bool tc_cols = MODE == kCastRHT && a.colwise != 0;
   uint32_t tmem = 0;
   if (tc_cols) {
-    fill_hadamard_operand(sm.hmat, a.sign_mask);
+    fill_hadamard_operand(sm.hmat, kScRegion, a.sign_mask);
     fence_proxy_async_shared();  // the operand, before the tensor cores read it
     if (tid == 0) {
       mbar_init(sm.mma_bar, 1);
@@ -241,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
       if (tc_cols) {
         tc_done = true;
         const int warp = tid >> 5;
-        if (ok && tid == 0) rht_issue_mma(st, sm, tmem);
+        if (ok && tid == 0) rht_issue_mma(smem_u32(st), smem_u32(sm.hmat), kScRegion, tmem, sm.mma_bar);
         if (ok && warp < 4) {
           if (do_row)
             wide_pass_any<kCast1D>(smem_u32(st), sm.rtab_row, smem_u32(sm.sc_row + parity * kScRegion),
@@ -251,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, TileCfg<T>::kMinBlocks)
           const bool done = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(sm.mma_bar, (uint32_t)(k & 1), a.status));
           if (done) {
             tcgen05_after_sync();
-            rht_col_epilogue(tmem, sm, a, r0, c0, g_col, parity);
+            rht_col_epilogue<false>(tmem, warp & 3, sm.rtab_col, sm.sc_col + parity * kScRegion, a, r0, c0, g_col);
           } else {
             *sm.abort_flag = 1;
           }

@@ -25,6 +25,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "grid.cuh"
 #include "kernels.h"
 #include "tile_ops.cuh"
 
@@ -129,60 +130,6 @@ __device__ __forceinline__ FSmem fcarve(uint8_t* raw) {
   s.abort_flag = reinterpret_cast<int*>(s.amax + 1);
   s.pre = reinterpret_cast<uint16_t*>(s.abort_flag + 1);
   return s;
-}
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_release_add_gpu(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_relaxed_max_gpu(unsigned* p, unsigned v) {
-  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Grid-wide barrier and maximum.  Generation-counted, so the workspace needs
-// no clearing between calls: call g (its generation read at kernel start)
-// uses the pair arrive[g & 1] / maxbits[g & 1].  The last warp of each CTA
-// to finish phase A (a shared-memory count) publishes the CTA's maximum with
-// a relaxed atomic max, then arrives with a release add (which orders the
-// max before it); thread 0 of each CTA polls the count (acquire, bounded)
-// and then reads the maximum.  CTA 0 clears the other pair, which the next
-// call uses, and advances the generation, which the next call (ordered after
-// this kernel) reads.
-__device__ __forceinline__ void grid_arrive(SinglePassWorkspace* ws, unsigned gen, float warp_max) {
-  red_relaxed_max_gpu(&ws->maxbits[gen & 1u], __float_as_uint(warp_max));
-  red_release_add_gpu(&ws->arrive[gen & 1u], 1u);
-}
-// Thread 0 only; false when the wait ran out.
-__device__ __forceinline__ bool grid_wait_max(SinglePassWorkspace* ws, unsigned gen, unsigned expected,
-                                              unsigned* status, float* out) {
-  const long long t0 = clock64();
-  while (ld_acquire_gpu(&ws->arrive[gen & 1u]) < expected) {
-    if (clock64() - t0 > kWaitLimitCycles) {
-      atomicOr(status, kStatusGridTimeout);
-      return false;
-    }
-  }
-  *out = __uint_as_float(ld_relaxed_gpu(&ws->maxbits[gen & 1u]));
-  if (blockIdx.x == 0) {  // unused by this call; the next one counts there
-    ws->arrive[(gen + 1u) & 1u] = 0u;
-    ws->maxbits[(gen + 1u) & 1u] = 0u;
-    st_release_gpu(&ws->gen, gen + 1u);
-  }
-  return true;
 }
 
 // max|x| over this warp's share of a staged tile: BF16, a quarter of the

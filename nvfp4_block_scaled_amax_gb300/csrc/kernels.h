@@ -76,7 +76,8 @@ struct SinglePassWorkspace {
   unsigned pad0;
   unsigned arrive[2];
   unsigned maxbits[2];
-  unsigned pad[10];
+  unsigned maxbits2[2];  // a second maximum (the Hadamard quantize: max|RHT(x)|)
+  unsigned pad[8];
 };
 constexpr size_t kSinglePassHeaderBytes = 64;
 static_assert(sizeof(SinglePassWorkspace) == kSinglePassHeaderBytes, "workspace header layout");
@@ -85,6 +86,10 @@ static_assert(sizeof(SinglePassWorkspace) == kSinglePassHeaderBytes, "workspace 
 // args.amax_col) and the fused cast (1D or 2D), x read from HBM once.
 cudaError_t launch_single_pass(const void* x, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
                                const LaunchCtx& ctx);
+// The same for the Hadamard quantize (BF16): max|x| into args.amax_row,
+// max|RHT(x)| into args.amax_col, then the row-wise cast of x and the
+// column-wise cast of the transformed columns.
+cudaError_t launch_single_pass_rht(const void* x, CastArgs args, SinglePassWorkspace* ws, const LaunchCtx& ctx);
 // CTAs the single-pass kernel uses for an M x N input.
 int single_pass_grid(int64_t M, int64_t N, const LaunchCtx& ctx);
 

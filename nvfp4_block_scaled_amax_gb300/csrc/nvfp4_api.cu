@@ -307,6 +307,44 @@ nvfp4_status nvfp4_quantize_2d_single_pass(const void* x, int dtype, int64_t M, 
   return quantize_single_pass(kCast2D, x, dtype, M, N, out, flags, noop, workspace, stream);
 }
 
+nvfp4_status nvfp4_quantize_rht_single_pass(const void* x, int dtype, int64_t M, int64_t N,
+                                            const nvfp4_output* out, unsigned flags, uint32_t sign_mask,
+                                            const float* noop, void* workspace, void* stream) {
+  if (!(flags & NVFP4_COLWISE))  // rows of x only: the transform plays no part
+    return quantize_single_pass(kCast1D, x, dtype, M, N, out, flags, noop, workspace, stream);
+  const unsigned allowed = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SWIZZLED;
+  nvfp4_status st = check_quantize(x, dtype, M, N, out, flags, allowed);
+  if (st != NVFP4_OK) return st;
+  if (dtype != NVFP4_BF16) return NVFP4_ERR_DTYPE;
+  if (M % 16 != 0 || N % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (workspace == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(workspace) || (noop != nullptr && !aligned16(noop))) return NVFP4_ERR_ALIGN;
+  LaunchCtx ctx;
+  if ((st = make_ctx(stream, &ctx)) != NVFP4_OK) return st;
+  const bool row = flags & NVFP4_ROWWISE;
+  if (M == 0 || N == 0) {
+    // nothing to cast: both maxima of an empty tensor are 0
+    return from_cuda(launch_amax(x, true, 0, row ? out->amax_row : out->amax_col, row ? out->amax_col : nullptr,
+                                 noop, ctx));
+  }
+  CastArgs a = {};
+  a.M = M;
+  a.N = N;
+  a.data_row = row ? out->data_row : nullptr;
+  a.scale_row = row ? out->scale_row : nullptr;
+  a.amax_row = row ? out->amax_row : nullptr;
+  a.data_col = out->data_col;
+  a.scale_col = out->scale_col;
+  a.amax_col = out->amax_col;
+  a.noop = noop;
+  a.status = ctx.status;
+  a.rowwise = row;
+  a.colwise = 1;
+  a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
+  a.sign_mask = sign_mask & 0xFFFFu;
+  return from_cuda(launch_single_pass_rht(x, a, static_cast<SinglePassWorkspace*>(workspace), ctx));
+}
+
 nvfp4_status nvfp4_quantize_row_scaled(const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,
                                        unsigned flags, const float* noop, void* stream) {
   const unsigned allowed = NVFP4_ROWWISE | NVFP4_SWIZZLED | NVFP4_SKIP_AMAX;

@@ -107,6 +107,13 @@ def test_single_pass_validation(lib):
         assert fn(X, 0, 256, 256, ctypes.byref(o), ROW | SKIP, None, A, None) == ERR_FLAGS        # no skip-amax
         assert fn(X, 0, 192, 256, ctypes.byref(o), ROW | COL | SWZ, None, A, None) == ERR_ALIGN
     assert lib.nvfp4_quantize_2d_single_pass(X, 0, 24, 256, ctypes.byref(o), ROW, None, A, None) == ERR_SHAPE
+    rht = lib.nvfp4_quantize_rht_single_pass
+    assert rht(X, 0, 256, 256, ctypes.byref(o), ROW | COL, 0, None, None, None) == ERR_NULL      # workspace
+    assert rht(X, 0, 256, 256, ctypes.byref(o), ROW | COL, 0, None, A + 4, None) == ERR_ALIGN
+    assert rht(X, 0, 256, 256, ctypes.byref(o), ROW | COL | SKIP, 0, None, A, None) == ERR_FLAGS
+    assert rht(X, 1, 256, 256, ctypes.byref(o), ROW | COL, 0, None, A, None) == ERR_DTYPE       # BF16 only
+    assert rht(X, 0, 24, 256, ctypes.byref(o), ROW | COL, 0, None, A, None) == ERR_SHAPE
+    assert rht(X, 0, 192, 256, ctypes.byref(o), ROW | COL | SWZ, 0, None, A, None) == ERR_ALIGN
 
 
 def test_amax_and_misc_validation(lib):

@@ -68,18 +68,49 @@ def test_single_pass_workspace_reuse(oracle_mod, mode):
 
 
 @pytest.mark.parametrize("M,N", [(16, 16), (128, 128), (48, 80), (208, 336), (384, 640), (1088, 1024)])
-def test_rht_matches_oracle(oracle_mod, M, N):
+@pytest.mark.parametrize("path", ["two_pass", "single_pass"])
+def test_rht_matches_oracle(oracle_mod, M, N, path):
     x = _x(M, N, torch.bfloat16, seed=M + 3 * N, kind="outliers")
     mask = inputs.sign_mask_from_seed(M + N)
     ref = oracle_mod.quantize("rht", bits(x), sign_mask=mask)
     for swizzled in ([False, True] if (M % 128 == 0 and N % 128 == 0) else [False]):
-        q = nv.quantize(x.cuda(), "rht", sign_mask=mask, swizzled=swizzled)
+        q = nv.quantize(x.cuda(), "rht", sign_mask=mask, swizzled=swizzled, path=path)
         torch.cuda.synchronize()
         assert_quantize_equal(oracle_mod, q, ref, swizzled, rowwise=True, colwise=False, what="rht row")
         np.testing.assert_array_equal(np_(q.amax_col), ref["amax_col"])
         sc_ref = oracle_mod.swizzle(ref["col_scale"]) if swizzled else ref["col_scale"].reshape(-1)
         nd, ns = compare_rht_codes(np_(q.data_col), ref["col_data"], np_(q.scale_col), sc_ref)
         assert nd <= max(1, 1e-4 * M * N) and ns <= nd
+
+
+def test_rht_single_pass_reuse_and_reloads(oracle_mod):
+    """Single-pass Hadamard quantize over repeated calls on one workspace,
+    shapes with several tiles per CTA (phase-B reloads of tiles that did not
+    stay in shared memory), both amaxes and the dual-amax reuse sequence."""
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    calls = 0
+    for it, (M, N) in enumerate([(4096, 4352), (128, 128), (1040, 2064), (2048, 1024)]):
+        base = _x(M, N, torch.bfloat16, seed=40 + it, kind="outliers")
+        mask = inputs.sign_mask_from_seed(it)
+        seq = inputs.reuse_sequence(base) if M * N <= 4 << 20 else [base]
+        for x in seq:
+            ref = oracle_mod.quantize("rht", bits(x), sign_mask=mask)
+            for swizzled in ([False, True] if (M % 128 == 0 and N % 128 == 0) else [False]):
+                q = nv.quantize(x.cuda(), "rht", sign_mask=mask, swizzled=swizzled, path="single_pass",
+                                workspace=ws)
+                torch.cuda.synchronize()
+                calls += 1
+                assert_quantize_equal(oracle_mod, q, ref, swizzled, rowwise=True, colwise=False,
+                                      what=f"rht {M}x{N} call {calls}")
+                np.testing.assert_array_equal(np_(q.amax_col), ref["amax_col"])
+                sc_ref = oracle_mod.swizzle(ref["col_scale"]) if swizzled else ref["col_scale"].reshape(-1)
+                nd, ns = compare_rht_codes(np_(q.data_col), ref["col_data"], np_(q.scale_col), sc_ref)
+                assert nd <= max(1, 1e-4 * M * N) and ns <= nd
+    w = ws.view(torch.int32).cpu()
+    assert int(w[0]) == calls                       # one generation per call
+    assert int(w[2 + (calls & 1)]) == 0             # the next call's arrival count is clear
+    assert int(w[4 + (calls & 1)]) == 0 and int(w[6 + (calls & 1)]) == 0   # and both its maxima
+    assert nv.device_status() == 0
 
 
 @pytest.mark.parametrize("M,N", [(16, 16), (40, 64), (128, 128), (300, 4096), (256, 6144), (64, 2048)])
