@@ -352,6 +352,14 @@ def bench_variants(nv, inputs, args, dev, flush, stream):
         ms = statistics.median(time_steps(step, steps, flush, stream))
         gbs = workload_bytes(spec) / (ms / 1e3) / 1e9
         out[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        if spec["mode"] == "rht":  # the single-pass alternative (x read from HBM once)
+            sp = lambda: nv.quantize(x, "rht", swizzled=spec["swizzled"], sign_mask=mask, out=q,  # noqa
+                                     path="single_pass")
+            for _ in range(3):
+                sp()
+            sms = statistics.median(time_steps(sp, steps, flush, stream))
+            sgbs = workload_bytes(spec) / (sms / 1e3) / 1e9
+            out[name + "_single_pass"] = {"ms": round(sms, 5), "GB/s": round(sgbs, 1), "frac": round(sgbs / peak, 4)}
         if spec["mode"] in ("2d", "1d") and spec["M"] == 8192:
             dq = lambda: nv.dequantize(q.data_row, q.scale_row, q.amax_row, swizzled=spec["swizzled"])  # noqa
             for _ in range(3):
