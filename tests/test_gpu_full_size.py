@@ -83,6 +83,23 @@ def test_2d_8192x5120_swizzled_with_dequant(oracle_mod):
 
 
 @pytest.mark.parametrize("swizzled", [False, True])
+def test_2d_single_pass_many_tiles_per_cta(oracle_mod, swizzled):
+    # 16384x5120: 5120 tiles, 34 per CTA on 152 SMs -- more than the 2D
+    # single-pass kernel keeps tile maxima for, so phase B finds them again;
+    # most tiles are re-read in phase B
+    x = inputs.randn(16384, 5120, seed=11)
+    q = nv.quantize(x.cuda(), "2d", swizzled=swizzled, path="single_pass")
+    torch.cuda.synchronize()
+    xb = bits(x)
+    M, N = xb.shape
+    assert np_(q.amax_row)[0] == oracle_mod.amax(xb)
+    rows = _sample(M, 32, 7, must=(0, 16, M - 1))
+    cols = _sample(N, 32, 8, must=(0, N - 1))
+    _check_sampled(oracle_mod, q, xb, "2d", rows, cols, swizzled)
+    assert nv.device_status() == 0
+
+
+@pytest.mark.parametrize("swizzled", [False, True])
 def test_row_scaled_16384x4096(oracle_mod, swizzled):
     spec = inputs.WORKLOADS["rowscaled_16384x4096_bf16"]
     x = inputs.make(spec)
@@ -100,11 +117,12 @@ def test_row_scaled_16384x4096(oracle_mod, swizzled):
     assert bool((q.data_row[torch.from_numpy(zero).cuda()] == 0).all())
 
 
-def test_rht_8192x8192(oracle_mod):
+@pytest.mark.parametrize("path", ["two_pass", "single_pass"])
+def test_rht_8192x8192(oracle_mod, path):
     spec = inputs.WORKLOADS["rht_8192x8192_bf16"]
     x = inputs.make(spec)
     mask = inputs.sign_mask_from_seed(spec["seed"])
-    q = nv.quantize(x.cuda(), "rht", sign_mask=mask, swizzled=False)
+    q = nv.quantize(x.cuda(), "rht", sign_mask=mask, swizzled=False, path=path)
     torch.cuda.synchronize()
     xb = bits(x)
     assert np_(q.amax_row)[0] == oracle_mod.amax(xb)
