@@ -21,12 +21,13 @@
 //     reverse order (most recently read first, so mostly from L2; phase A
 //     marked them evict-last), writing codes, and scales in the compact or
 //     cuBLAS 128x4 layout.
-// x is read from HBM once; the call is one launch.
-#include <atomic>
-
+// x is read from HBM once; the call is one launch.  The stage ring, the
+// scale write-back and the cooperative launch are shared with fused_rht.cu
+// (single_pass.cuh).
 #include "common.cuh"
 #include "grid.cuh"
 #include "kernels.h"
+#include "single_pass.cuh"
 #include "tile_ops.cuh"
 
 namespace nvfp4 {
@@ -179,37 +180,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int G = gridDim.x, b = blockIdx.x;
   const int n = (a.num_tiles - 1 - b) / G + 1;  // tiles t_k = b + k * G, k < n (grid <= tiles)
   const int kept_from = n > S ? n - S : 0;      // tiles k >= kept_from stay staged after phase A
-  auto tile_rc = [&](int k, int64_t& r0, int64_t& c0) {
-    const int t = b + k * G;
-    const int tr = t / a.tiles_n, tc = t - tr * a.tiles_n;
-    r0 = (int64_t)tr * kTile;
-    c0 = (int64_t)tc * kTile;
-  };
+  const sp::StageRing<T, S, WPT> ring{sm.stages, sm.full, sm.loaded, sm.issued, sm.tile_in, &tmap, b, G,
+                                      a.tiles_n, a.status};
 
-  const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   // Loads: phase A reads tiles 0..n-1 (the ones reloaded in phase B are kept
   // in L2 with evict-last), phase B reloads tiles kept_from-1 .. 0.
-  auto issue = [&](int k, uint64_t pol) {
-    const int s = k % S;
-    int64_t r0, c0;
-    tile_rc(k, r0, c0);
-    uint8_t* dst = sm.stages + (size_t)s * tile_bytes<T>();
-    sm.issued[s] += 1;
-    *reinterpret_cast<volatile int*>(&sm.tile_in[s]) = k;  // before the arrival (see wait_full)
-    mbar_arrive_expect_tx(&sm.full[s], tile_bytes<T>());
-#pragma unroll
-    for (int bb = 0; bb < TileCfg<T>::kBoxes; ++bb)
-      tma_load_2d(dst + bb * kBoxBytes, &tmap, (int32_t)c0 + bb * TileCfg<T>::kBoxCols, (int32_t)r0, &sm.full[s],
-                  pol);
-  };
+  const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   if (tid == 0) {
     *sm.gen = ld_acquire_gpu(&ws->gen);  // this call's barrier generation
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&sm.full[s], 1);
-      sm.loaded[s] = 0;
-      sm.issued[s] = 0;
-      sm.tile_in[s] = -1;
-    }
+    ring.init();
     for (int q = 0; q < 2 * kGroups; ++q) {
       sm.staged[q] = 0;
       sm.wb[q] = 0;
@@ -220,82 +199,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     *sm.cta_in = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap);
-    for (int k = 0; k < S && k < n; ++k) issue(k, k >= kept_from ? stream : keep);
+    for (int k = 0; k < S && k < n; ++k) ring.issue(k, k >= kept_from ? stream : keep);
   }
   __syncthreads();
 
-  // A warp done reading stage s's tile data counts itself; the last of the
-  // group's warps loads tile `next` (if any) into the stage.  The count's
-  // address depends on `token`, a value computed from every word the warp
-  // read (warp-wide registers), so the count cannot be performed before
-  // those reads have completed.
-  auto release_data = [&](int s, int next, uint64_t pol, uint32_t token) {
-    if (lane == 0) {
-      uint32_t zero;
-      asm volatile("and.b32 %0, %1, 0;" : "=r"(zero) : "r"(token));
-      if (atomicAdd(&sm.loaded[s] + zero, 1u) == (unsigned)(WPT - 1)) {
-        sm.loaded[s] = 0;
-        __threadfence_block();
-        if (next >= 0) issue(next, pol);
-      }
-    }
-  };
-  // Bounded wait of lane 0 until *slot == want (a shared-memory hand-over
-  // between warps); false when it ran out.
-  // Bounded wait of lane 0 until the counter *p reaches `want`.
-  auto wait_count = [&](const unsigned* p, unsigned want) {
-    unsigned good = 1;
-    if (lane == 0) {
-      const volatile unsigned* c = p;
-      if (*c < want) {
-        const long long t0 = clock64();
-        while (*c < want) {
-          if (clock64() - t0 > kWaitLimitCycles) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            good = 0;
-            break;
-          }
-        }
-      }
-    }
-    const bool ok = __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
-    __threadfence_block();  // the counted warps' shared-memory writes are visible past this point
-    return ok;
-  };
-  auto wait_slot = [&](const int* p, int want) {
-    unsigned good = 1;
-    if (lane == 0) {
-      const volatile int* slot = p;
-      if (*slot != want) {
-        const long long t0 = clock64();
-        while (*slot != want) {
-          if (clock64() - t0 > kWaitLimitCycles) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            good = 0;
-            break;
-          }
-        }
-      }
-    }
-    return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
-  };
-
   const int grp = warp / WPT, cw = warp % WPT;
   bool ok = true;
-  // Waits until tile k is in its stage.  The stage's previous tile belongs
-  // to another group, which may not be done with it yet: a parity wait
-  // issued before tile k's load would refer to that earlier phase.  So lane
-  // 0 first waits (bounded) until tile k's load has been issued (tile_in[s]
-  // is set before its arrival), which also means the earlier phase is
-  // complete.  Tile k's load is the stage's fill number k / S in phase A;
-  // in phase B a stage's tiles are reloaded in reverse order after its F
-  // phase-A fills, tile s + m S as fill 2F - 2 - m: the parity is (k / S) & 1
-  // in both phases.
-  auto wait_full = [&](int k) {
-    const int s = k % S;
-    if (!wait_slot(&sm.tile_in[s], k)) return false;
-    return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.full[s], (uint32_t)((k / S) & 1), a.status)) != 0;
-  };
 
   // phase A: max|x| of this group's tiles (k == grp mod kGroups)
   constexpr bool kPre = MODE == kCast2D && sizeof(T) == 2;
@@ -303,7 +212,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   float m = 0.0f;
   for (int k = grp; k < n; k += kGroups) {
     const int s = k % S;
-    if (!wait_full(k)) {
+    if (!ring.wait_full(k)) {
       ok = false;
       break;
     }
@@ -312,16 +221,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       // the wide partition of phase B: record the tile's 16x16 maxima
       SubW sw;
       const int wr = cw >> 1, wc = cw & 1, i = lane >> 2, j = lane & 3;
-      load_sub_w(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), wc, 64 * wr + 8 * i, j, i & 1, sw);
+      load_sub_w(ring.stage(s), wc, 64 * wr + 8 * i, j, i & 1, sw);
       uint32_t acc;
       mk = wide_tile_max(sw.a, sw.b, acc);
       if ((i & 1) == 0) sm.pre[k * 64 + (4 * wr + (i >> 1)) * 8 + 4 * wc + j] = (uint16_t)(__float_as_uint(mk) >> 16);
     } else {
-      mk = share_absmax<T>(smem_u32(sm.stages + (size_t)s * tile_bytes<T>()), cw);
+      mk = share_absmax<T>(ring.stage(s), cw);
     }
     m = fmaxf(m, mk);
     if (k + S < n)  // tile k leaves shared memory: load tile k + S into its stage
-      release_data(s, k + S, k + S >= kept_from ? stream : keep, __float_as_uint(mk));
+      ring.release(s, k + S, k + S >= kept_from ? stream : keep, __float_as_uint(mk));
   }
   if (!ok) *sm.abort_flag = 1;
 #pragma unroll
@@ -352,9 +261,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   if (*sm.abort_flag) {
     // let this CTA's copies in flight (the last load into each stage) land,
     // bounded, before leaving
-    if (tid == 0)
-      for (int s = 0; s < S; ++s)
-        if (sm.issued[s] > 0) mbar_wait_bounded(&sm.full[s], (sm.issued[s] - 1u) & 1u, a.status);
+    if (tid == 0) ring.drain();
     return;
   }
   const float g = *sm.amax;
@@ -376,51 +283,35 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const volatile int* abort_flag = sm.abort_flag;
   auto buffer = [&](int it) { return sm.sc + (size_t)((grp * 2 + (it & 1)) * 2) * kScRegion; };
   // this warp's share of tile kk's (iteration it's) scale write-back
-  auto write_back_share = [&](int kk, int it) {
+  auto write_back = [&](int kk, int it) {
     const int q = grp * 2 + (it & 1);
-    if (!wait_count(&sm.staged[q], (unsigned)(WPT * ((it >> 1) + 1)))) return false;
     int64_t r0, c0;
-    tile_rc(kk, r0, c0);
-    const uint8_t* sc = buffer(it);
-    const int per = a.swizzled ? 64 / WPT : 128 / WPT;  // 16-byte lines or rows per warp
-    if (lane < per) {
-      const int t = cw * per + lane;
-      if (do_row) store_scale_tile<MODE, false>(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
-      if (do_col)
-        store_scale_tile<MODE, true>(sc + kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
-    }
-    __syncwarp();  // the lanes' reads of the buffer are complete (their stores used them)
-    if (lane == 0) atomicAdd(&sm.wb[q], 1u);
-    return true;
+    ring.tile_rc(kk, r0, c0);
+    return sp::write_back_share<MODE, WPT>(buffer(it), &sm.staged[q], &sm.wb[q], (unsigned)(WPT * ((it >> 1) + 1)),
+                                           cw, a, r0, c0, do_row, do_col);
   };
   int it = 0, k_prev = -1;
   int pending_q = -1;  // lane 0, kBulk: buffer of the copies this warp issued, not yet freed
-  auto free_pending = [&] {
-    if (kBulk && lane == 0 && pending_q >= 0) {
-      bulk_wait_read_all();
-      __threadfence_block();
-      atomicAdd(&sm.wb[pending_q], (unsigned)WPT);
-      pending_q = -1;
-    }
-  };
   for (int k = k_top; k >= 0; k -= kGroups, ++it) {
     const int s = k % S;
-    free_pending();
+    if constexpr (kBulk) sp::bulk_free<WPT>(pending_q, sm.wb);
     if (*abort_flag) break;
-    if (k < kept_from && !wait_full(k)) {  // a wait ran out: outputs unfinished
+    if (k < kept_from && !ring.wait_full(k)) {  // a wait ran out: outputs unfinished
       *sm.abort_flag = 1;
       break;
     }
     int64_t r0, c0;
-    tile_rc(k, r0, c0);
+    ring.tile_rc(k, r0, c0);
     uint8_t* sc = buffer(it);
-    const uint32_t st = smem_u32(sm.stages + (size_t)s * tile_bytes<T>());
+    const uint32_t st = ring.stage(s);
     const unsigned* wbq = &sm.wb[grp * 2 + (it & 1)];
     bool scales_ok = true;
     // the buffer's previous contents (iteration it - 2) are written back
-    auto scale_wait = [&] { scales_ok = wait_count(wbq, (unsigned)(WPT * (it >> 1))) && scales_ok; };
+    auto scale_wait = [&] {
+      scales_ok = sp::warp_wait_count(wbq, (unsigned)(WPT * (it >> 1)), a.status) && scales_ok;
+    };
     if constexpr (sizeof(T) == 2) {
-      const auto hooks = make_hooks([&](uint32_t token) { release_data(s, k - S, stream, token); }, scale_wait,
+      const auto hooks = make_hooks([&](uint32_t token) { ring.release(s, k - S, stream, token); }, scale_wait,
                                     use_pre ? sm.pre + k * 64 : nullptr);
       wide_pass_any<MODE, kBulk>(st, sm.rtab_row, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, do_row,
                                  do_col, cw, hooks);
@@ -430,7 +321,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                               g, do_row, do_col, cw);
       __syncwarp();
       __threadfence_block();  // the warp's reads of the stage are done
-      release_data(s, k - S, stream, 0u);
+      ring.release(s, k - S, stream, 0u);
     }
     if (!scales_ok) {  // a wait ran out: outputs unfinished
       *sm.abort_flag = 1;
@@ -440,76 +331,31 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       // The group's last warp to finish staging writes the tile's scales
       // with one bulk copy per direction; the buffer is freed once the
       // copies have read it (at that warp's next iteration).
-      fence_proxy_async_shared();  // this lane's staging stores, before the copy engine reads them
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        const int q = grp * 2 + (it & 1);
-        if (atomicAdd(&sm.staged[q], 1u) % WPT == (unsigned)(WPT - 1)) {
-          __threadfence_block();
-          if (do_row)
-            bulk_store(a.scale_row + ((r0 >> 7) * (a.N >> 6) + (c0 >> 6)) * 512, smem_u32(sc), 1024);
-          if (do_col)
-            bulk_store(a.scale_col + ((c0 >> 7) * (a.M >> 6) + (r0 >> 6)) * 512, smem_u32(sc + kScRegion), 1024);
-          bulk_commit();
-          pending_q = q;
-        }
-      }
-      __syncwarp();
+      sp::bulk_staged<WPT>(&sm.staged[grp * 2 + (it & 1)], grp * 2 + (it & 1), sc, a, r0, c0, do_row, do_col,
+                           pending_q);
     } else {
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();  // this warp's staged scales before its count
-        atomicAdd(&sm.staged[grp * 2 + (it & 1)], 1u);
-      }
-      if (k_prev >= 0 && !write_back_share(k_prev, it - 1)) {
+      sp::count_staged(&sm.staged[grp * 2 + (it & 1)]);
+      if (k_prev >= 0 && !write_back(k_prev, it - 1)) {
         *sm.abort_flag = 1;
         break;
       }
       k_prev = k;
     }
   }
-  if (k_prev >= 0 && !*abort_flag && !write_back_share(k_prev, it - 1)) *sm.abort_flag = 1;
+  if (!kBulk && k_prev >= 0 && !*abort_flag && !write_back(k_prev, it - 1)) *sm.abort_flag = 1;
   if constexpr (kBulk) {
-    free_pending();
+    sp::bulk_free<WPT>(pending_q, sm.wb);
     if (lane == 0) bulk_wait_all();  // this warp's scale copies (if any) are complete
   }
   // After an abort, the last warp to leave lets the copies still in flight
   // (the latest load into each stage) land, bounded, before the CTA exits.
   __syncwarp();
-  if (lane == 0 && atomicAdd(&sm.exited[0], 1u) == (unsigned)(kWarps - 1) && *abort_flag) {
-    for (int s = 0; s < S; ++s)
-      if (sm.issued[s] > 0) mbar_wait_bounded(&sm.full[s], (sm.issued[s] - 1u) & 1u, a.status);
-  }
+  if (lane == 0 && atomicAdd(&sm.exited[0], 1u) == (unsigned)(kWarps - 1) && *abort_flag) ring.drain();
 }
 
 template <typename T, int MODE, bool kBulk>
 cudaError_t launch_fused_t(const CUtensorMap& map, const CastArgs& a, SinglePassWorkspace* ws, const LaunchCtx& ctx) {
-  auto fn = fused_kernel<T, MODE, kBulk>;
-  static std::atomic<uint64_t> attr_set{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fused_smem_bytes<T>());
-    if (e != cudaSuccess) return e;
-    attr_set.fetch_or(bit);
-  }
-  const int grid = a.num_tiles < ctx.num_sms ? a.num_tiles : ctx.num_sms;
-  if (grid == 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kFusedThreads);
-  cfg.dynamicSmemBytes = fused_smem_bytes<T>();
-  cfg.stream = ctx.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (grid barrier)
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  void* args[] = {(void*)&map, (void*)&a, (void*)&ws};
-  return cudaLaunchKernelExC(&cfg, (const void*)fn, args);
+  return sp::launch_persistent<fused_kernel<T, MODE, kBulk>>(fused_smem_bytes<T>(), kFusedThreads, map, a, ws, ctx);
 }
 
 }  // namespace

@@ -5,21 +5,21 @@
 // buffers", review reply: with RHT the row amax is max|x| and the column
 // amax is max|RHT(x)|).
 //
-// The structure of fused.cu (one CTA per SM, cooperative launch, 16 warps in
+// The structure of fused.cu, with the same stage ring and scale write-back
+// (single_pass.cuh): one CTA per SM, cooperative launch, 16 warps in
 // 4 groups of 4, a 6-stage TMA ring, phase A / grid barrier / phase B, the
-// last 6 tiles of a CTA resident), with the transform on the tensor cores
+// last 6 tiles of a CTA resident.  The transform runs on the tensor cores
 // (hadamard.cuh): every tile's eight 16-row blocks are transformed by
 // tcgen05.mma into the group's 128 tensor-memory columns (4 groups x 128 =
 // all 512), once in phase A for the column amax and again in phase B for the
 // cast, so x is read from HBM once and the transform never leaves the chip.
 // In both phases warp cw of a group reads tensor-memory lanes 32 cw .. +31
 // (tile columns), the lane quarter its warp index allows.
-#include <atomic>
-
 #include "common.cuh"
 #include "grid.cuh"
 #include "hadamard.cuh"
 #include "kernels.h"
+#include "single_pass.cuh"
 #include "tile_ops.cuh"
 
 namespace nvfp4 {
@@ -112,27 +112,7 @@ struct RowHooks {  // the row-wise wide pass: the stage is released after the co
   __device__ __forceinline__ void data_done(uint32_t token) const { *tok ^= token; }
   __device__ __forceinline__ void scale_wait() const;
 };
-// Bounded wait of lane 0 until *c >= want; warp-uniform result.
-__device__ __forceinline__ bool warp_wait_count(const unsigned* p, unsigned want, unsigned* status) {
-  unsigned good = 1;
-  if ((threadIdx.x & 31) == 0) {
-    const volatile unsigned* c = p;
-    if (*c < want) {
-      const long long t0 = clock64();
-      while (*c < want) {
-        if (clock64() - t0 > kWaitLimitCycles) {
-          atomicOr(status, kStatusWaitTimeout);
-          good = 0;
-          break;
-        }
-      }
-    }
-  }
-  const bool ok = __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
-  __threadfence_block();
-  return ok;
-}
-__device__ __forceinline__ void RowHooks::scale_wait() const { *ok = warp_wait_count(wbq, want, status) && *ok; }
+__device__ __forceinline__ void RowHooks::scale_wait() const { *ok = sp::warp_wait_count(wbq, want, status) && *ok; }
 
 template <bool kBulk>
 __global__ void __launch_bounds__(kRThreads, 1)
@@ -146,36 +126,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int G = gridDim.x, b = blockIdx.x;
   const int n = (a.num_tiles - 1 - b) / G + 1;  // tiles t_k = b + k * G, k < n (grid <= tiles)
   const int kept_from = n > S ? n - S : 0;
-  auto tile_rc = [&](int k, int64_t& r0, int64_t& c0) {
-    const int t = b + k * G;
-    const int tr = t / a.tiles_n, tc = t - tr * a.tiles_n;
-    r0 = (int64_t)tr * kTile;
-    c0 = (int64_t)tc * kTile;
-  };
+  const sp::StageRing<uint16_t, S, WPT> ring{sm.stages, sm.full, sm.loaded, sm.issued, sm.tile_in, &tmap, b, G,
+                                             a.tiles_n, a.status};
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
-  auto issue = [&](int k, uint64_t pol) {
-    const int s = k % S;
-    int64_t r0, c0;
-    tile_rc(k, r0, c0);
-    uint8_t* dst = sm.stages + (size_t)s * tile_bytes<uint16_t>();
-    sm.issued[s] += 1;
-    *reinterpret_cast<volatile int*>(&sm.tile_in[s]) = k;  // before the arrival (see wait_full)
-    mbar_arrive_expect_tx(&sm.full[s], tile_bytes<uint16_t>());
-#pragma unroll
-    for (int bb = 0; bb < TileCfg<uint16_t>::kBoxes; ++bb)
-      tma_load_2d(dst + bb * kBoxBytes, &tmap, (int32_t)c0 + bb * TileCfg<uint16_t>::kBoxCols, (int32_t)r0,
-                  &sm.full[s], pol);
-  };
   fill_hadamard_operand(sm.hmat, 256, a.sign_mask);
   fence_proxy_async_shared();  // the operand, before the tensor cores read it
   if (tid == 0) {
     *sm.gen = ld_acquire_gpu(&ws->gen);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&sm.full[s], 1);
-      sm.loaded[s] = 0;
-      sm.issued[s] = 0;
-      sm.tile_in[s] = -1;
-    }
+    ring.init();
     for (int q = 0; q < kGroups; ++q) {
       mbar_init(&sm.mma_bar[q], 1);
       sm.tfree[q] = 0;
@@ -191,48 +149,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
     *sm.cta_in = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap);
-    for (int k = 0; k < S && k < n; ++k) issue(k, k >= kept_from ? stream : keep);
+    for (int k = 0; k < S && k < n; ++k) ring.issue(k, k >= kept_from ? stream : keep);
   }
   if (warp == 0) tmem_alloc(sm.tmem_slot, kTmemCols);
   tcgen05_before_sync();
   __syncthreads();
   tcgen05_after_sync();
   const uint32_t tmem_all = *reinterpret_cast<volatile uint32_t*>(sm.tmem_slot);
-
-  auto release_data = [&](int s, int next, uint64_t pol, uint32_t token) {
-    if (lane == 0) {
-      uint32_t zero;
-      asm volatile("and.b32 %0, %1, 0;" : "=r"(zero) : "r"(token));
-      if (atomicAdd(&sm.loaded[s] + zero, 1u) == (unsigned)(WPT - 1)) {
-        sm.loaded[s] = 0;
-        __threadfence_block();
-        if (next >= 0) issue(next, pol);
-      }
-    }
-  };
-  auto wait_slot = [&](const int* p, int want) {
-    unsigned good = 1;
-    if (lane == 0) {
-      const volatile int* slot = p;
-      if (*slot != want) {
-        const long long t0 = clock64();
-        while (*slot != want) {
-          if (clock64() - t0 > kWaitLimitCycles) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            good = 0;
-            break;
-          }
-        }
-      }
-    }
-    return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
-  };
-  // tile k's load into its stage (see fused.cu: parity (k / S) & 1 in both phases)
-  auto wait_full = [&](int k) {
-    const int s = k % S;
-    if (!wait_slot(&sm.tile_in[s], k)) return false;
-    return __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.full[s], (uint32_t)((k / S) & 1), a.status)) != 0;
-  };
 
   const int grp = warp / WPT, cw = warp % WPT;
   const uint32_t tmem = tmem_all + 128u * (uint32_t)grp;  // the group's columns
@@ -242,7 +165,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   // all four warps have read the group's previous transform.
   auto transform = [&](uint32_t st) {
     if (cw != 0) return true;
-    if (!warp_wait_count(&sm.tfree[grp], (unsigned)(WPT * jt), a.status)) return false;
+    if (!sp::warp_wait_count(&sm.tfree[grp], (unsigned)(WPT * jt), a.status)) return false;
     if (lane == 0) rht_issue_mma(st, smem_u32(sm.hmat), 256, tmem, &sm.mma_bar[grp]);
     ++mma_issued;
     return true;
@@ -269,11 +192,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
   float m_row = 0.0f, m_col = 0.0f;
   for (int k = grp; k < n; k += kGroups) {
     const int s = k % S;
-    if (!wait_full(k)) {
+    if (!ring.wait_full(k)) {
       ok = false;
       break;
     }
-    const uint32_t st = smem_u32(sm.stages + (size_t)s * tile_bytes<uint16_t>());
+    const uint32_t st = ring.stage(s);
     if (!transform(st)) {
       ok = false;
       break;
@@ -288,7 +211,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     m_row = fmaxf(m_row, mr);
     m_col = fmaxf(m_col, mc);
     if (k + S < n)  // tile k leaves shared memory (the transform has read it too)
-      release_data(s, k + S, k + S >= kept_from ? stream : keep, __float_as_uint(mr) ^ __float_as_uint(mc));
+      ring.release(s, k + S, k + S >= kept_from ? stream : keep, __float_as_uint(mr) ^ __float_as_uint(mc));
   }
   if (!ok) *sm.abort_flag = 1;
 #pragma unroll
@@ -337,45 +260,27 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int k_top = n - 1 - ((n - 1 - grp) % kGroups + kGroups) % kGroups;
   const volatile int* abort_flag = sm.abort_flag;
   auto buffer = [&](int it) { return sm.sc + (size_t)((grp * 2 + (it & 1)) * 2) * kScRegion; };
-  auto write_back_share = [&](int kk, int it) {
+  auto write_back = [&](int kk, int it) {
     const int q = grp * 2 + (it & 1);
-    if (!warp_wait_count(&sm.staged[q], (unsigned)(WPT * ((it >> 1) + 1)), a.status)) return false;
     int64_t r0, c0;
-    tile_rc(kk, r0, c0);
-    const uint8_t* sc = buffer(it);
-    const int per = a.swizzled ? 64 / WPT : 128 / WPT;
-    if (lane < per) {
-      const int t = cw * per + lane;
-      if (do_row) store_scale_tile<kCast1D, false>(sc, a.scale_row, r0, c0 / 16, a.M, a.N / 16, a.swizzled, t);
-      if (do_col)
-        store_scale_tile<kCast1D, true>(sc + kScRegion, a.scale_col, c0, r0 / 16, a.N, a.M / 16, a.swizzled, t);
-    }
-    __syncwarp();
-    if (lane == 0) atomicAdd(&sm.wb[q], 1u);
-    return true;
+    ring.tile_rc(kk, r0, c0);
+    return sp::write_back_share<kCast1D, WPT>(buffer(it), &sm.staged[q], &sm.wb[q],
+                                              (unsigned)(WPT * ((it >> 1) + 1)), cw, a, r0, c0, do_row, do_col);
   };
   int it = 0, k_prev = -1;
   int pending_q = -1;  // lane 0, kBulk: buffer of the copies this warp issued, not yet freed
-  auto free_pending = [&] {
-    if (kBulk && lane == 0 && pending_q >= 0) {
-      bulk_wait_read_all();
-      __threadfence_block();
-      atomicAdd(&sm.wb[pending_q], (unsigned)WPT);
-      pending_q = -1;
-    }
-  };
   for (int k = early_exit ? -1 : k_top; k >= 0; k -= kGroups, ++it) {
     const int s = k % S;
-    free_pending();
+    if constexpr (kBulk) sp::bulk_free<WPT>(pending_q, sm.wb);
     if (*abort_flag) break;
-    if (k < kept_from && !wait_full(k)) {
+    if (k < kept_from && !ring.wait_full(k)) {
       *sm.abort_flag = 1;
       break;
     }
     int64_t r0, c0;
-    tile_rc(k, r0, c0);
+    ring.tile_rc(k, r0, c0);
     uint8_t* sc = buffer(it);
-    const uint32_t st = smem_u32(sm.stages + (size_t)s * tile_bytes<uint16_t>());
+    const uint32_t st = ring.stage(s);
     bool good = true;
     if (do_col) good = transform(st);
     uint32_t tok = 0;
@@ -392,44 +297,26 @@ __global__ void __launch_bounds__(kRThreads, 1)
         good = false;
       transform_done();
     }
-    release_data(s, k - S, stream, tok);
+    ring.release(s, k - S, stream, tok);
     if (!good) {
       *sm.abort_flag = 1;
       break;
     }
     if constexpr (kBulk) {
-      fence_proxy_async_shared();  // this lane's staging stores, before the copy engine reads them
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        const int q = grp * 2 + (it & 1);
-        if (atomicAdd(&sm.staged[q], 1u) % WPT == (unsigned)(WPT - 1)) {
-          __threadfence_block();
-          if (do_row)
-            bulk_store(a.scale_row + ((r0 >> 7) * (a.N >> 6) + (c0 >> 6)) * 512, smem_u32(sc), 1024);
-          if (do_col)
-            bulk_store(a.scale_col + ((c0 >> 7) * (a.M >> 6) + (r0 >> 6)) * 512, smem_u32(sc + kScRegion), 1024);
-          bulk_commit();
-          pending_q = q;
-        }
-      }
-      __syncwarp();
+      sp::bulk_staged<WPT>(&sm.staged[grp * 2 + (it & 1)], grp * 2 + (it & 1), sc, a, r0, c0, do_row, do_col,
+                           pending_q);
     } else {
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        atomicAdd(&sm.staged[grp * 2 + (it & 1)], 1u);
-      }
-      if (k_prev >= 0 && !write_back_share(k_prev, it - 1)) {
+      sp::count_staged(&sm.staged[grp * 2 + (it & 1)]);
+      if (k_prev >= 0 && !write_back(k_prev, it - 1)) {
         *sm.abort_flag = 1;
         break;
       }
       k_prev = k;
     }
   }
-  if (!kBulk && k_prev >= 0 && !*abort_flag && !write_back_share(k_prev, it - 1)) *sm.abort_flag = 1;
+  if (!kBulk && k_prev >= 0 && !*abort_flag && !write_back(k_prev, it - 1)) *sm.abort_flag = 1;
   if constexpr (kBulk) {
-    free_pending();
+    sp::bulk_free<WPT>(pending_q, sm.wb);
     if (lane == 0) bulk_wait_all();
   }
   // A transform this warp issued and nobody waited for (after an abort) ends
@@ -446,39 +333,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
     // after an abort, lets the CTA's copies still in flight land (bounded)
     tcgen05_after_sync();
     tmem_dealloc(tmem_all, kTmemCols);
-    if (lane == 0 && *abort_flag)
-      for (int s = 0; s < S; ++s)
-        if (sm.issued[s] > 0) mbar_wait_bounded(&sm.full[s], (sm.issued[s] - 1u) & 1u, a.status);
+    if (lane == 0 && *abort_flag) ring.drain();
   }
 }
 
 template <bool kBulk>
 cudaError_t launch_rht_t(const CUtensorMap& map, const CastArgs& a, SinglePassWorkspace* ws, const LaunchCtx& ctx) {
-  auto fn = fused_rht_kernel<kBulk>;
-  static std::atomic<uint64_t> attr_set{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rht_smem_bytes());
-    if (e != cudaSuccess) return e;
-    attr_set.fetch_or(bit);
-  }
-  const int grid = a.num_tiles < ctx.num_sms ? a.num_tiles : ctx.num_sms;
-  if (grid == 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kRThreads);
-  cfg.dynamicSmemBytes = rht_smem_bytes();
-  cfg.stream = ctx.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (grid barrier)
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  void* args[] = {(void*)&map, (void*)&a, (void*)&ws};
-  return cudaLaunchKernelExC(&cfg, (const void*)fn, args);
+  return sp::launch_persistent<fused_rht_kernel<kBulk>>(rht_smem_bytes(), kRThreads, map, a, ws, ctx);
 }
 
 }  // namespace
