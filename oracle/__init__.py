@@ -227,6 +227,33 @@ def quantize(mode: str, x: np.ndarray, rowwise: bool = True, colwise: bool = Tru
             "col_data": col_data, "col_scale": col_scale, "amax_col": amax_col}
 
 
+def quantize_grouped(mode: str, x: np.ndarray, splits, rowwise: bool = True, colwise: bool = True) -> list[dict]:
+    """Grouped (multi-tensor) quantize: x stacks G tensors along its first
+    dimension, tensor g being rows [sum(splits[:g]), sum(splits[:g+1])) with
+    the common last dimension N.  Each member is quantized as a tensor of its
+    own: its own amax (so its own global scale), block scales and codes, and
+    its column-wise output is the transpose of its own rows only.
+
+    Reading of "Implement row-scaled NVFP4 fprop recipe" (Important Files
+    Changed, grouped_tensor_storage.py): a grouped tensor keeps its members'
+    amaxes side by side and slices them per member tensor, so every member
+    carries its own amax.  Modes 1d and 2d (row-scaled needs no grouping: each
+    row is already a tensor of its own).  Returns one ``quantize`` result per
+    member, in order.
+    """
+    x = np.ascontiguousarray(x)
+    if mode not in ("1d", "2d"):
+        raise ValueError("grouped quantize: modes 1d and 2d")
+    splits = [int(m) for m in splits]
+    if any(m < 0 for m in splits) or sum(splits) != x.shape[0]:
+        raise ValueError("grouped quantize: splits must be non-negative and sum to the rows of x")
+    out, r = [], 0
+    for m in splits:
+        out.append(quantize(mode, x[r:r + m], rowwise=rowwise, colwise=colwise))
+        r += m
+    return out
+
+
 def swizzle_offset(r: int, c: int, C: int) -> int:
     return int(lib().oracle_swizzle_offset(r, c, C))
 

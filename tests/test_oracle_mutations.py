@@ -119,3 +119,54 @@ def test_unaltered_copy_passes_the_pins(outcomes):
 def test_planted_mistake_fails_a_pin(outcomes, name):
     rc, tail = outcomes[name]
     assert rc == 1, f"{name}: pins passed or errored (rc={rc})\n{tail}"
+
+
+# Planted mistakes in the grouped (multi-tensor) composition, which is Python:
+# each altered version of ``quantize_grouped`` must fail one of the grouped
+# pins of ``test_oracle_quantize.py``.
+def _grouped_mutants(oracle):
+    def shared_amax(mode, x, splits, rowwise=True, colwise=True):
+        a = oracle.amax(x)
+        out, r = [], 0
+        for m in splits:
+            out.append(oracle.quantize(mode, x[r:r + m], rowwise=rowwise, colwise=colwise, amax=(a, a)))
+            r += m
+        return out
+
+    def rows_from_zero(mode, x, splits, rowwise=True, colwise=True):
+        return [oracle.quantize(mode, x[:m], rowwise=rowwise, colwise=colwise) for m in splits]
+
+    def columns_of_whole_tensor(mode, x, splits, rowwise=True, colwise=True):
+        whole = oracle.quantize(mode, x, rowwise=False, colwise=colwise)
+        out, r = [], 0
+        for m in splits:
+            o = oracle.quantize(mode, x[r:r + m], rowwise=rowwise, colwise=colwise)
+            if colwise and m:
+                o["col_data"] = whole["col_data"][:, r // 2:(r + m) // 2]
+                o["col_scale"] = whole["col_scale"][:, r // 16:(r + m) // 16]
+            out.append(o)
+            r += m
+        return out
+
+    return {"shared_amax": shared_amax, "rows_from_zero": rows_from_zero,
+            "columns_of_whole_tensor": columns_of_whole_tensor}
+
+
+@pytest.mark.parametrize("name", ["shared_amax", "rows_from_zero", "columns_of_whole_tensor"])
+def test_planted_grouped_mistake_fails_a_pin(name):
+    import types
+
+    import oracle
+    import test_oracle_quantize as pins
+
+    fake = types.SimpleNamespace(**{k: getattr(oracle, k) for k in dir(oracle) if not k.startswith("__")})
+    fake.quantize_grouped = _grouped_mutants(oracle)[name]
+    checks = [pins.test_grouped_members_match_restatement, pins.test_grouped_2d_member_matches_restatement,
+              pins.test_grouped_single_member_is_the_plain_quantize, pins.test_grouped_members_are_independent]
+    failed = 0
+    for check in checks:
+        try:
+            check(fake)
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    assert failed > 0, f"no grouped pin caught {name}"

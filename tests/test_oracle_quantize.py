@@ -392,3 +392,79 @@ def test_shape_domain(oracle_mod):
     # an empty tensor has amax 0 and no codes
     out = oracle_mod.quantize("1d", np.zeros((0, 32), np.float32), colwise=False)
     assert out["amax_row"][0] == 0.0 and out["row_data"].shape == (0, 16)
+
+
+# ---------------------------------------------------------------------------
+# grouped (multi-tensor) quantize: each member is a tensor of its own
+# ---------------------------------------------------------------------------
+
+def test_grouped_members_match_restatement(oracle_mod):
+    """Each member against the numpy restatement on its own rows, with the
+    amax of its own rows (a member scaled far above the others shows whether
+    the amax is shared)."""
+    splits = [32, 0, 16, 48]
+    x = inputs.randn(sum(splits), 64, seed=41, dtype=torch.float32).numpy()
+    x[48:96] *= np.float32(1000.0)
+    outs = oracle_mod.quantize_grouped("1d", x, splits)
+    assert len(outs) == len(splits)
+    r = 0
+    for m, out in zip(splits, outs):
+        X = x[r:r + m]
+        a = np.float32(np.abs(X).max()) if m else np.float32(0)
+        assert out["amax_row"][0] == a and out["amax_col"][0] == a
+        if m:
+            g = np_global(a)
+            d, s = np_quantize_1d_rows(X, np.full(m, g, np.float32))
+            np.testing.assert_array_equal(out["row_data"], d)
+            np.testing.assert_array_equal(out["row_scale"], s)
+            dT, sT = np_quantize_1d_rows(np.ascontiguousarray(X.T), np.full(64, g, np.float32))
+            np.testing.assert_array_equal(out["col_data"], dT)
+            np.testing.assert_array_equal(out["col_scale"], sT)
+        else:
+            assert out["row_data"].shape == (0, 32) and out["col_data"].shape == (64, 0)
+        r += m
+
+
+def test_grouped_2d_member_matches_restatement(oracle_mod):
+    splits = [16, 64]
+    x = bf16_bits(inputs.outliers(80, 96, seed=42, frac=0.02))
+    outs = oracle_mod.quantize_grouped("2d", x, splits)
+    X = to_f32(x)[16:80]
+    d, s = np_quantize_2d_rows(X, np_global(np.abs(X).max()))
+    np.testing.assert_array_equal(outs[1]["row_data"], d)
+    np.testing.assert_array_equal(outs[1]["row_scale"], s)
+    np.testing.assert_array_equal(outs[1]["col_data"], nibble_transpose(d, 64, 96))
+
+
+def test_grouped_single_member_is_the_plain_quantize(oracle_mod):
+    x = bf16_bits(inputs.randn(48, 80, seed=43))
+    for mode in ("1d", "2d"):
+        (one,) = oracle_mod.quantize_grouped(mode, x, [48])
+        ref = oracle_mod.quantize(mode, x)
+        for key in ("row_data", "row_scale", "amax_row", "col_data", "col_scale", "amax_col"):
+            np.testing.assert_array_equal(one[key], ref[key])
+
+
+def test_grouped_members_are_independent(oracle_mod):
+    """Scaling one member by 2^k changes only that member's amax: every code
+    and scale of every member stays the same (power-of-two invariance of a
+    member that owns its amax)."""
+    splits = [16, 32, 16]
+    x = inputs.randn(64, 48, seed=44, dtype=torch.float32).numpy()
+    base = oracle_mod.quantize_grouped("1d", x, splits)
+    y = x.copy()
+    y[16:48] *= np.float32(2.0 ** 9)
+    moved = oracle_mod.quantize_grouped("1d", y, splits)
+    for g, (b, m) in enumerate(zip(base, moved)):
+        for key in ("row_data", "row_scale", "col_data", "col_scale"):
+            np.testing.assert_array_equal(m[key], b[key])
+        factor = np.float32(2.0 ** 9) if g == 1 else np.float32(1.0)
+        assert m["amax_row"][0] == b["amax_row"][0] * factor
+
+
+def test_grouped_rejects_bad_splits(oracle_mod):
+    x = np.zeros((32, 16), np.float32)
+    with pytest.raises(ValueError):
+        oracle_mod.quantize_grouped("1d", x, [16, 8])
+    with pytest.raises(ValueError):
+        oracle_mod.quantize_grouped("rht", x, [32])
