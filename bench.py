@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -56,25 +57,40 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(source: str) -> str:
+    """Hash of what a kernel is built from: its source file in csrc/, the
+    local headers it includes (transitively) and the build script (flags)."""
+    pkg = os.path.join(ROOT, "nvfp4_block_scaled_amax_gb300")
+    dirs = [os.path.join(pkg, "csrc"), os.path.join(ROOT, "include")]
+    seen, todo = {}, [source]
+    while todo:
+        name = todo.pop()
+        if name in seen:
+            continue
+        path = next((os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name))), None)
+        if path is None:
+            continue
+        with open(path, "rb") as f:
+            seen[name] = f.read()
+        todo += re.findall(r'#include "([^"]+)"', seen[name].decode())
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "nvfp4_block_scaled_amax_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for name in sorted(seen):
+        h.update(name.encode() + seen[name])
+    with open(os.path.join(pkg, "build.py"), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
     """DRAM bytes per call from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current sources of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    if not e or e.get("kernel_hash") != kernel_source_hash(e.get("source", "")):
         return None
     return e.get("dram_bytes_per_call")
 
@@ -370,6 +386,23 @@ def bench_variants(nv, inputs, args, dev, flush, stream):
                                       "frac": round(dbytes / (dms / 1e3) / 1e9 / peak, 4)}
         del x, q
         torch.cuda.empty_cache()
+    # grouped quantize: the members of inputs.GROUPED (8192 x 5120 in all),
+    # each with its own amax, in three launches
+    spec = inputs.GROUPED
+    splits, N = spec["splits"], spec["N"]
+    x = inputs.make_grouped(spec).to(dev)
+    outs = [nv.empty(m, N, swizzled=spec["swizzled"], device=dev) for m in splits]
+    gstep = lambda: nv.quantize_grouped(x, splits, spec["mode"], swizzled=spec["swizzled"], out=outs)  # noqa
+    for _ in range(3):
+        gstep()
+    gms = statistics.median(time_steps(gstep, steps, flush, stream))
+    dt = "bf16" if spec["dtype"] == torch.bfloat16 else "fp32"
+    gbytes = sum(splits) * N * BYTES_PER_ELEM[(dt, "rowcol")]
+    gname = f"grouped_{len(splits)}_members_{sum(splits)}x{N}_{dt}_{spec['mode']}"
+    out[gname] = {"ms": round(gms, 5), "GB/s": round(gbytes / (gms / 1e3) / 1e9, 1),
+                  "frac": round(gbytes / (gms / 1e3) / 1e9 / peak, 4)}
+    del x, outs
+    torch.cuda.empty_cache()
     return out
 
 

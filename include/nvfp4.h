@@ -152,6 +152,35 @@ nvfp4_status nvfp4_quantize_row_scaled(const void* x, int dtype, int64_t M, int6
                                        const float* noop, void* stream);
 
 /*
+ * Grouped (multi-tensor) 1D / 2D quantize: x (row-major, N columns) stacks
+ * num_groups member tensors along its first dimension, member g being the
+ * group_rows[g] rows that follow the earlier members' rows.  Every member is
+ * quantized as a tensor of its own into outs[g] (the buffers and layouts of
+ * nvfp4_quantize_1d / _2d for a group_rows[g] x N tensor): its own amax, so
+ * its own global scale ("Implement row-scaled NVFP4 fprop recipe", Important
+ * Files Changed: a grouped tensor keeps one amax slice per member), and its
+ * column-wise output is the transpose of its own rows.  Three launches
+ * whatever num_groups (zero the amaxes, max|x| per member, one cast over all
+ * members' tiles).
+ *   group_rows, outs: HOST arrays of num_groups entries, read before the call
+ *   returns (the device buffers they name stay the caller's).
+ *   1 <= num_groups <= NVFP4_MAX_GROUPS; group_rows[g] >= 0 (0: an empty
+ *   member, amax 0); N % 16 == 0; with COLWISE, or for 2D, group_rows[g] %
+ *   16 == 0; with SWIZZLED, group_rows[g] % 128 == 0 and N % 128 == 0.
+ *   Every member's outputs are checked as nvfp4_quantize_1d checks them, and
+ *   no two amax buffers of the call may be the same (NVFP4_ERR_FLAGS).
+ *   flags: ROWWISE | COLWISE | SWIZZLED | SKIP_AMAX, for every member.
+ *   Validation fails before anything is enqueued.
+ */
+#define NVFP4_MAX_GROUPS 64
+nvfp4_status nvfp4_quantize_grouped_1d(const void* x, int dtype, int64_t N, int num_groups,
+                                       const int64_t* group_rows, const nvfp4_output* outs,
+                                       unsigned flags, const float* noop, void* stream);
+nvfp4_status nvfp4_quantize_grouped_2d(const void* x, int dtype, int64_t N, int num_groups,
+                                       const int64_t* group_rows, const nvfp4_output* outs,
+                                       unsigned flags, const float* noop, void* stream);
+
+/*
  * NVFP4 quantize with the random Hadamard transform on the column-wise path
  * ("Write both NVFP4 amax buffers", GPU work per quantize call: the RHT path
  * runs a zeroing kernel, a Hadamard-amax kernel and the quantize kernel;

@@ -10,7 +10,8 @@ Hadamard transform, dequantize) runs in the library's CUDA kernels.
 
 Modes: "1d" (1x16 blocks), "2d" (16x16 tiles), "rht" (random Hadamard
 transform on the column-wise path) and "row_scaled" (one amax per row,
-row-wise only).
+row-wise only).  ``quantize_grouped`` quantizes several tensors stacked along
+the first dimension, each with its own amax, in three launches.
 
 Paths for "1d" / "2d" / "rht": "single_pass" (one persistent kernel: amax,
 grid barrier, cast; x read from HBM once; needs a small workspace, which
@@ -38,7 +39,7 @@ FP32 = 1
 
 __all__ = ["NVFP4Tensor", "NVFP4Error", "empty", "compute_amax", "compute_amax_rht", "quantize",
            "single_pass_workspace", "reset_workspaces",
-           "quantize_1d", "quantize_2d", "quantize_rht", "quantize_row_scaled", "dequantize",
+           "quantize_1d", "quantize_2d", "quantize_rht", "quantize_row_scaled", "quantize_grouped", "dequantize",
            "swizzle_scales", "scale_bytes", "device_status"]
 
 
@@ -230,6 +231,45 @@ def quantize(x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: b
         else:
             raise ValueError(f"unknown mode {mode!r}")
     _lib.check(rc, f"nvfp4 quantize ({mode})")
+    return out
+
+
+def quantize_grouped(x: torch.Tensor, splits, mode: str = "1d", rowwise: bool = True, colwise: bool = True,
+                     swizzled: bool = False, out: list[NVFP4Tensor] | None = None, skip_amax: bool = False,
+                     noop: torch.Tensor | None = None) -> list[NVFP4Tensor]:
+    """Grouped (multi-tensor) quantize: x (M x N, bfloat16 or float32) stacks
+    len(splits) member tensors along its first dimension, member g being the
+    splits[g] rows after the earlier members'.  Each member is quantized as a
+    tensor of its own (its own amax, its own transpose) into its own
+    NVFP4Tensor; three kernel launches whatever the number of members.
+    mode: "1d" or "2d".  out: one NVFP4Tensor per member (default: allocated)."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (M x N)")
+    if mode not in ("1d", "2d"):
+        raise ValueError("grouped quantize: mode '1d' or '2d'")
+    splits = [int(m) for m in splits]
+    if not 1 <= len(splits) <= _lib.MAX_GROUPS:
+        raise ValueError(f"grouped quantize: 1 to {_lib.MAX_GROUPS} members")
+    if sum(splits) != x.shape[0]:
+        raise ValueError("grouped quantize: splits must sum to the rows of x")
+    N = x.shape[1]
+    if out is None:
+        out = [empty(m, N, rowwise, colwise, swizzled=swizzled, device=x.device) for m in splits]
+    if len(out) != len(splits):
+        raise ValueError("grouped quantize: one output per member")
+    for q in out:
+        q.swizzled = swizzled
+        _require_cuda(q.data_row, q.scale_row, q.amax_row, q.data_col, q.scale_col, q.amax_col)
+    _require_cuda(x, noop)
+    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLED if swizzled else 0) | \
+        (SKIP_AMAX if skip_amax else 0)
+    rows = (ctypes.c_int64 * len(splits))(*splits)
+    outs = (_lib.Output * len(out))(*[q.c_struct() for q in out])
+    L = _lib.load()
+    fn = L.nvfp4_quantize_grouped_1d if mode == "1d" else L.nvfp4_quantize_grouped_2d
+    with _OnDevice(x.device):
+        rc = fn(_ptr(x), _dtype_code(x), N, len(splits), rows, outs, flags, _ptr(noop), _stream(x.device))
+    _lib.check(rc, f"nvfp4 grouped quantize ({mode})")
     return out
 
 

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "grouped.h"
 #include "kernels.h"
 #include "nvfp4.h"
 
@@ -189,6 +190,65 @@ nvfp4_status quantize_single_pass(int mode, const void* x, int dtype, int64_t M,
                                       static_cast<SinglePassWorkspace*>(workspace), ctx));
 }
 
+static_assert(NVFP4_MAX_GROUPS == kMaxGroups, "member table size");
+
+// Grouped quantize: every member is checked as a plain quantize of its rows
+// (its slice of x and its outputs), then the member table is filled.
+nvfp4_status quantize_grouped(int mode, const void* x, int dtype, int64_t N, int num_groups,
+                              const int64_t* group_rows, const nvfp4_output* outs, unsigned flags,
+                              const float* noop, void* stream) {
+  if (group_rows == nullptr || outs == nullptr) return NVFP4_ERR_NULL;
+  if (num_groups < 1 || num_groups > kMaxGroups) return NVFP4_ERR_SHAPE;
+  if (dtype != NVFP4_BF16 && dtype != NVFP4_FP32) return NVFP4_ERR_DTYPE;
+  if (N < 0 || N >= kMaxDim || N % 16 != 0) return NVFP4_ERR_SHAPE;
+  const unsigned allowed = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SWIZZLED | NVFP4_SKIP_AMAX;
+  const bool row = flags & NVFP4_ROWWISE, col = flags & NVFP4_COLWISE;
+  const int64_t eb = dtype == NVFP4_BF16 ? 2 : 4;
+  GroupedArgs ga = {};
+  int64_t total = 0;
+  for (int g = 0; g < num_groups; ++g) {
+    const int64_t rows = group_rows[g];
+    if (rows < 0 || rows >= kMaxDim) return NVFP4_ERR_SHAPE;
+    if ((col || mode == kCast2D) && rows % 16 != 0) return NVFP4_ERR_SHAPE;
+    const void* xg = x == nullptr ? nullptr : static_cast<const char*>(x) + total * N * eb;
+    nvfp4_status st = check_quantize(xg, dtype, rows, N, &outs[g], flags, allowed);
+    if (st != NVFP4_OK) return st;
+    ga.row0[g] = total;
+    ga.rows[g] = rows;
+    ga.data_row[g] = row ? outs[g].data_row : nullptr;
+    ga.scale_row[g] = row ? outs[g].scale_row : nullptr;
+    ga.amax_row[g] = row ? outs[g].amax_row : nullptr;
+    ga.data_col[g] = col ? outs[g].data_col : nullptr;
+    ga.scale_col[g] = col ? outs[g].scale_col : nullptr;
+    ga.amax_col[g] = col ? outs[g].amax_col : nullptr;
+    total += rows;
+    if (total >= kMaxDim) return NVFP4_ERR_SHAPE;
+  }
+  // Each member owns its amax buffers: two members that shared one would
+  // merge their maxima.
+  const float* seen[2 * kMaxGroups];
+  int n_seen = 0;
+  for (int g = 0; g < num_groups; ++g)
+    for (const float* p : {static_cast<const float*>(ga.amax_row[g]), static_cast<const float*>(ga.amax_col[g])}) {
+      if (p == nullptr) continue;
+      for (int i = 0; i < n_seen; ++i)
+        if (seen[i] == p) return NVFP4_ERR_FLAGS;
+      seen[n_seen++] = p;
+    }
+  if (noop != nullptr && !aligned16(noop)) return NVFP4_ERR_ALIGN;
+  LaunchCtx ctx;
+  nvfp4_status st = make_ctx(stream, &ctx);
+  if (st != NVFP4_OK) return st;
+  ga.num_groups = num_groups;
+  ga.N = N;
+  ga.noop = noop;
+  ga.status = ctx.status;
+  ga.rowwise = row;
+  ga.colwise = col;
+  ga.swizzled = (flags & NVFP4_SWIZZLED) != 0;
+  return from_cuda(launch_grouped(x, dtype == NVFP4_BF16, mode, total, ga, (flags & NVFP4_SKIP_AMAX) != 0, ctx));
+}
+
 }  // namespace
 
 // The host-side checks of the single-pass entry points (everything before
@@ -361,6 +421,18 @@ nvfp4_status nvfp4_quantize_row_scaled(const void* x, int dtype, int64_t M, int6
   }
   return from_cuda(launch_row_scaled(x, dtype == NVFP4_BF16, M, N, out->data_row, out->scale_row, out->amax_row,
                                      (flags & NVFP4_SKIP_AMAX) != 0, (flags & NVFP4_SWIZZLED) != 0, noop, ctx));
+}
+
+nvfp4_status nvfp4_quantize_grouped_1d(const void* x, int dtype, int64_t N, int num_groups,
+                                       const int64_t* group_rows, const nvfp4_output* outs, unsigned flags,
+                                       const float* noop, void* stream) {
+  return quantize_grouped(kCast1D, x, dtype, N, num_groups, group_rows, outs, flags, noop, stream);
+}
+
+nvfp4_status nvfp4_quantize_grouped_2d(const void* x, int dtype, int64_t N, int num_groups,
+                                       const int64_t* group_rows, const nvfp4_output* outs, unsigned flags,
+                                       const float* noop, void* stream) {
+  return quantize_grouped(kCast2D, x, dtype, N, num_groups, group_rows, outs, flags, noop, stream);
 }
 
 nvfp4_status nvfp4_dequantize(const uint8_t* data, const uint8_t* scale, const float* amax, int64_t rows,

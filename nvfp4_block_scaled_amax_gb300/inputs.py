@@ -106,6 +106,31 @@ WORKLOADS = {
 }
 
 
+# Grouped quantize (tensors stacked along the first dimension, each with its
+# own amax): eight members of uneven height, multiples of 128, 8192 rows in
+# all, N = 5120; member g is N(0, 1) times 10^e_g, e_g drawn from the seed in
+# [-3, 3] (members of different magnitude, like the per-expert inputs of a
+# mixture-of-experts layer).
+GROUPED = dict(mode="1d", splits=[1280, 768, 1152, 896, 1024, 1408, 640, 1024], N=5120, dtype=torch.bfloat16,
+               seed=8, swizzled=True)
+
+
+def make_grouped(spec=None, splits=None, N: int | None = None) -> torch.Tensor:
+    """Builds the stacked input of a grouped workload (optionally with other
+    member heights or N)."""
+    spec = GROUPED if spec is None else spec
+    splits = spec["splits"] if splits is None else list(splits)
+    N = spec["N"] if N is None else N
+    g = _gen(spec["seed"])
+    x = torch.randn((sum(splits), N), generator=g, dtype=torch.float32)
+    e = torch.randint(-3, 4, (len(splits),), generator=g)
+    r = 0
+    for m, k in zip(splits, e.tolist()):
+        x[r:r + m] *= float(10.0 ** k)
+        r += m
+    return x.to(spec["dtype"])
+
+
 def make(name_or_spec, M: int | None = None, N: int | None = None) -> torch.Tensor:
     """Builds the input of a named workload (optionally at another shape)."""
     spec = WORKLOADS[name_or_spec] if isinstance(name_or_spec, str) else name_or_spec

@@ -134,6 +134,51 @@ def test_amax_and_misc_validation(lib):
     assert lib.nvfp4_device_status(None, 0) == ERR_NULL
 
 
+def test_grouped_validation(lib):
+    from nvfp4_block_scaled_amax_gb300._lib import Output
+
+    def members(n, over=None):
+        over = over or {}
+        outs = (Output * n)()
+        for g in range(n):
+            base = 0x1000000 * (g + 1)
+            d = dict(data_row=base, scale_row=base + 0x100000, amax_row=base + 0x200000,
+                     data_col=base + 0x300000, scale_col=base + 0x400000, amax_col=base + 0x500000)
+            d.update(over.get(g, {}))
+            outs[g] = Output(**d)
+        return outs
+
+    def grouped(rows, o=None, fn=lib.nvfp4_quantize_grouped_1d, x=X, dtype=0, N=256, flags=ROW | COL, n=None,
+                noop=None):
+        r = (ctypes.c_int64 * len(rows))(*rows)
+        o = members(len(rows)) if o is None else o
+        return fn(x, dtype, N, len(rows) if n is None else n, r, o, flags, noop, None)
+
+    r = (ctypes.c_int64 * 1)(128)
+    assert lib.nvfp4_quantize_grouped_1d(X, 0, 256, 1, None, members(1), ROW, None, None) == ERR_NULL
+    assert lib.nvfp4_quantize_grouped_1d(X, 0, 256, 1, r, None, ROW, None, None) == ERR_NULL
+    assert grouped([128], n=0) == ERR_SHAPE                          # at least one member
+    assert grouped([128] * 65) == ERR_SHAPE                          # at most 64
+    assert grouped([128, -16]) == ERR_SHAPE
+    assert grouped([128, 24]) == ERR_SHAPE                           # column blocks need rows % 16
+    assert grouped([128, 24], flags=ROW) != ERR_SHAPE                # row-wise 1D does not
+    assert grouped([128, 24], flags=ROW, fn=lib.nvfp4_quantize_grouped_2d) == ERR_SHAPE
+    assert grouped([128], N=24, flags=ROW) == ERR_SHAPE
+    assert grouped([128], dtype=2) == ERR_DTYPE
+    assert grouped([128], flags=0) == ERR_FLAGS
+    assert grouped([128], flags=ROW | ROWSC) == ERR_FLAGS
+    assert grouped([128, 64], flags=ROW | COL | SWZ) == ERR_ALIGN     # swizzle needs 128-row members
+    assert grouped([128], x=X + 8) == ERR_ALIGN
+    assert grouped([128], x=0) == ERR_NULL
+    assert grouped([0], x=0) != ERR_NULL                             # an empty member reads nothing
+    assert grouped([128, 128], o=members(2, {1: dict(scale_col=0)})) == ERR_NULL
+    assert grouped([128, 128], o=members(2, {1: dict(data_row=0x7)})) == ERR_ALIGN
+    shared = members(2, {1: dict(amax_row=0x1000000 + 0x200000)})  # member 1 reuses member 0's amax
+    assert grouped([128, 128], o=shared) == ERR_FLAGS
+    assert grouped([128], o=members(1, {0: dict(amax_col=0x1000000 + 0x200000)})) == ERR_FLAGS
+    assert grouped([128], noop=NOOP + 4) == ERR_ALIGN
+
+
 def test_python_layer_rejects_cpu_tensors():
     import torch
     import nvfp4_block_scaled_amax_gb300 as nv
