@@ -88,6 +88,16 @@ def lib() -> ctypes.CDLL:
                 vp, i64, vp, i64,
                 u8p, u8p, f32p, u8p, u8p, f32p]
             L.oracle_quantize.restype = ctypes.c_int
+            L.oracle_quantize_sr.argtypes = [
+                ctypes.c_int, vp, ctypes.c_int, i64, i64,
+                ctypes.c_int, ctypes.c_float, ctypes.c_float, vp,
+                vp, i64, vp, i64,
+                u8p, u8p, f32p, u8p, u8p, f32p]
+            L.oracle_quantize_sr.restype = ctypes.c_int
+            L.oracle_e2m1_sr_satfinite.argtypes = [ctypes.c_float, ctypes.c_uint8]
+            L.oracle_e2m1_sr_satfinite.restype = ctypes.c_uint8
+            L.oracle_e2m1_sr_array.argtypes = [vp, vp, vp, i64]
+            L.oracle_e2m1_sr_array.restype = None
             L.oracle_swizzle_offset.argtypes = [i64, i64, i64]
             L.oracle_swizzle_offset.restype = i64
             L.oracle_swizzle_scales.argtypes = [u8p, u8p, i64, i64]
@@ -119,6 +129,19 @@ def _dtype_code(x: np.ndarray) -> int:
 
 def e2m1(v: float) -> int:
     return int(lib().oracle_e2m1_rn_satfinite(float(v)))
+
+
+def e2m1_sr(v: float, rb: int) -> int:
+    """Stochastically rounded E2M1 code of v with random byte rb."""
+    return int(lib().oracle_e2m1_sr_satfinite(float(v), int(rb) & 0xFF))
+
+
+def e2m1_sr_array(v: np.ndarray, rb: np.ndarray) -> np.ndarray:
+    flat = np.ascontiguousarray(v, dtype=np.float32).ravel()
+    r = np.ascontiguousarray(np.broadcast_to(rb, np.shape(v)), dtype=np.uint8).ravel()
+    out = np.empty(flat.size, dtype=np.uint8)
+    lib().oracle_e2m1_sr_array(_ptr(flat), _ptr(r), _ptr(out), flat.size)
+    return out.reshape(np.shape(v))
 
 
 def e2m1_value(code: int) -> float:
@@ -189,7 +212,8 @@ def rht_amax(x: np.ndarray, mask: int) -> float:
 
 def quantize(mode: str, x: np.ndarray, rowwise: bool = True, colwise: bool = True,
              sign_mask: int = 0, amax: tuple[float, float] | None = None,
-             rows: np.ndarray | None = None, cols: np.ndarray | None = None) -> dict:
+             rows: np.ndarray | None = None, cols: np.ndarray | None = None,
+             rbits: np.ndarray | None = None) -> dict:
     """NVFP4-quantizes x (M x N; uint16 BF16 bits or float32).
 
     Returns compact outputs: ``row_data`` [nr, N/2], ``row_scale`` [nr, N/16],
@@ -197,7 +221,9 @@ def quantize(mode: str, x: np.ndarray, rowwise: bool = True, colwise: bool = Tru
     ``col_scale`` [nc, M/16], ``amax_col``.  ``rows`` / ``cols`` select which
     rows of the row-wise output and which columns of x (rows of the
     column-wise output) to produce; None means all.  ``amax`` = (row, col)
-    uses a given amax pair instead of reducing x.
+    uses a given amax pair instead of reducing x.  ``rbits`` (uint8, the
+    shape of x): stochastic rounding of the codes, modes 1d and 2d, element
+    (y, j) using rbits[y, j] in both outputs.
     """
     x = np.ascontiguousarray(x)
     M, N = x.shape
@@ -216,11 +242,21 @@ def quantize(mode: str, x: np.ndarray, rowwise: bool = True, colwise: bool = Tru
     amax_col = np.zeros(1, dtype=np.float32)
     given = amax is not None
     ar, ac = (amax if given else (0.0, 0.0))
-    rc = lib().oracle_quantize(
-        m, _ptr(x), _dtype_code(x), M, N, int(given), float(ar), float(ac), sign_mask & 0xFFFF,
-        _ptr(row_ids), n_row_arg, _ptr(col_ids), n_col_arg,
-        _ptr(row_data), _ptr(row_scale), _ptr(amax_row),
-        _ptr(col_data), _ptr(col_scale), _ptr(amax_col))
+    if rbits is None:
+        rc = lib().oracle_quantize(
+            m, _ptr(x), _dtype_code(x), M, N, int(given), float(ar), float(ac), sign_mask & 0xFFFF,
+            _ptr(row_ids), n_row_arg, _ptr(col_ids), n_col_arg,
+            _ptr(row_data), _ptr(row_scale), _ptr(amax_row),
+            _ptr(col_data), _ptr(col_scale), _ptr(amax_col))
+    else:
+        rb = np.ascontiguousarray(rbits, dtype=np.uint8)
+        if rb.shape != (M, N):
+            raise ValueError("rbits must hold one byte per element of x")
+        rc = lib().oracle_quantize_sr(
+            m, _ptr(x), _dtype_code(x), M, N, int(given), float(ar), float(ac), _ptr(rb),
+            _ptr(row_ids), n_row_arg, _ptr(col_ids), n_col_arg,
+            _ptr(row_data), _ptr(row_scale), _ptr(amax_row),
+            _ptr(col_data), _ptr(col_scale), _ptr(amax_col))
     if rc != 0:
         raise ValueError(f"oracle: shape {M}x{N} not defined for mode {mode}")
     return {"row_data": row_data, "row_scale": row_scale, "amax_row": amax_row[:max(nr, 1)],

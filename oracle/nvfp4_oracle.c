@@ -42,6 +42,17 @@
  * taken over i ascending and the result rounded to BF16 for BF16 input;
  * dequantize is ((E2M1(q) * float(s)) * (a / 2688)) in FP32, rounded to the
  * output type.
+ *
+ * Stochastic rounding (named by "Fuse NVFP4 scale swizzling on SM120 and
+ * SM121", Tests, as one axis of the comparisons; not otherwise described):
+ * read as stochastic rounding of the E2M1 codes only (block scales stay
+ * round-to-nearest-even), with the random numbers passed in: one random byte
+ * per element of x, used by both the row-wise and the column-wise code of
+ * that element.  For v = x * r with lo <= |v| < hi, lo and hi neighbouring
+ * E2M1 magnitudes, f = (|v| - lo) / (hi - lo): the magnitude rounds up to hi
+ * iff byte < 256 f, so P(up) = ceil(256 f) / 256 over a uniform byte (exactly
+ * f when f is a multiple of 1/256); |v| >= 6 saturates to 6; the sign of x is
+ * kept.
  */
 #include <float.h>
 #include <math.h>
@@ -111,6 +122,23 @@ uint8_t oracle_e2m1_rn_satfinite(float v) {
     }
   }
   return (uint8_t)(sign | (uint8_t)best);
+}
+
+/* E2M1 stochastic rounding with saturation (the reading above): the
+ * neighbours lo <= |v| < hi among the eight magnitudes, f = (|v| - lo) /
+ * (hi - lo), and the magnitude hi iff rb < 256 f.  |v| - lo, the division by
+ * the step (a power of two) and the product by 256 are exact in double, so
+ * the decision is exact.  A representable |v| (f = 0) never moves. */
+uint8_t oracle_e2m1_sr_satfinite(float v, uint8_t rb) {
+  uint8_t sign = signbit(v) ? 8u : 0u;
+  double m = fabs((double)v);
+  if (m >= 6.0) return (uint8_t)(sign | 7u);
+  int lo = 0;
+  for (int c = 1; c < 8; ++c)
+    if (E2M1_MAG[c] <= m) lo = c;
+  double f = (m - E2M1_MAG[lo]) / (E2M1_MAG[lo + 1] - E2M1_MAG[lo]);
+  int up = (double)rb < f * 256.0;
+  return (uint8_t)(sign | (uint8_t)(lo + up));
 }
 
 /* E4M3 (FN variant: bias 7, no infinities, 0x7F/0xFF = NaN, largest finite
@@ -205,9 +233,16 @@ static void put_code(uint8_t* row, int64_t j, uint8_t q) {
     row[j >> 1] = (uint8_t)((row[j >> 1] & 0xF0u) | q);
 }
 
+/* The code of p: round-to-nearest-even, or stochastic rounding with random
+ * byte rb[i * rb_stride] when rb is not NULL. */
+static uint8_t encode_elem(float p, const uint8_t* rb, int64_t rb_stride, int64_t i) {
+  return rb ? oracle_e2m1_sr_satfinite(p, rb[i * rb_stride]) : oracle_e2m1_rn_satfinite(p);
+}
+
 /* 1D quantization of one vector v[0..n) (n a multiple of 16) with global
- * encode scale g: one scale per 16 consecutive elements. */
-static void quantize_vector_1d(const float* v, int64_t n, float g,
+ * encode scale g: one scale per 16 consecutive elements.  rb: random bytes
+ * of the elements (element i at rb[i * rb_stride]), or NULL. */
+static void quantize_vector_1d(const float* v, int64_t n, float g, const uint8_t* rb, int64_t rb_stride,
                                uint8_t* data, uint8_t* scale) {
   for (int64_t k = 0; k < n / 16; ++k) {
     float b = 0.0f;
@@ -219,7 +254,7 @@ static void quantize_vector_1d(const float* v, int64_t n, float g,
     float r = oracle_encode_factor(s, g);
     for (int i = 0; i < 16; ++i) {
       float p = v[16 * k + i] * r;
-      put_code(data, 16 * k + i, oracle_e2m1_rn_satfinite(p));
+      put_code(data, 16 * k + i, encode_elem(p, rb, rb_stride, 16 * k + i));
     }
     scale[k] = s;
   }
@@ -228,8 +263,8 @@ static void quantize_vector_1d(const float* v, int64_t n, float g,
 /* 2D quantization of row y of a rows x cols matrix A (rows, cols multiples
  * of 16): each 16x16 tile has one scale from its max; row y's 1x16 blocks use
  * the scale of the tile they lie in. */
-static void quantize_row_2d(const float* A, int64_t cols, int64_t y, float g,
-                            uint8_t* data, uint8_t* scale) {
+static void quantize_row_2d(const float* A, int64_t cols, int64_t y, float g, const uint8_t* rb,
+                            int64_t rb_stride, uint8_t* data, uint8_t* scale) {
   int64_t y0 = (y / 16) * 16;
   for (int64_t k = 0; k < cols / 16; ++k) {
     float b = 0.0f;
@@ -242,7 +277,7 @@ static void quantize_row_2d(const float* A, int64_t cols, int64_t y, float g,
     float r = oracle_encode_factor(s, g);
     for (int i = 0; i < 16; ++i) {
       float p = A[y * cols + 16 * k + i] * r;
-      put_code(data, 16 * k + i, oracle_e2m1_rn_satfinite(p));
+      put_code(data, 16 * k + i, encode_elem(p, rb, rb_stride, 16 * k + i));
     }
     scale[k] = s;
   }
@@ -336,13 +371,13 @@ float oracle_rht_amax(const void* x, int dtype, int64_t M, int64_t N, uint32_t m
  *
  * Returns 0, or -1 on a shape the method does not define.
  */
-int oracle_quantize(int mode, const void* x, int dtype, int64_t M, int64_t N,
-                    int amax_given, float amax_row_in, float amax_col_in,
-                    uint32_t sign_mask,
-                    const int64_t* row_ids, int64_t n_row_ids,
-                    const int64_t* col_ids, int64_t n_col_ids,
-                    uint8_t* row_data, uint8_t* row_scale, float* amax_row_out,
-                    uint8_t* col_data, uint8_t* col_scale, float* amax_col_out) {
+static int quantize_impl(int mode, const void* x, int dtype, int64_t M, int64_t N,
+                         int amax_given, float amax_row_in, float amax_col_in,
+                         uint32_t sign_mask, const uint8_t* rbits,
+                         const int64_t* row_ids, int64_t n_row_ids,
+                         const int64_t* col_ids, int64_t n_col_ids,
+                         uint8_t* row_data, uint8_t* row_scale, float* amax_row_out,
+                         uint8_t* col_data, uint8_t* col_scale, float* amax_col_out) {
   int64_t nr = (n_row_ids < 0) ? M : n_row_ids;
   int64_t nc = (n_col_ids < 0) ? N : n_col_ids;
   if (M < 0 || N < 0) return -1;
@@ -350,6 +385,7 @@ int oracle_quantize(int mode, const void* x, int dtype, int64_t M, int64_t N,
   if (nc > 0 && M % 16 != 0) return -1;
   if (mode == MODE_2D && (M % 16 != 0 || N % 16 != 0)) return -1;
   if (mode == MODE_ROW_SCALED && nc > 0) return -1;
+  if (rbits && mode != MODE_1D && mode != MODE_2D) return -1;
 
   float* vec = (float*)malloc(sizeof(float) * (size_t)((M > N ? M : N) + 16));
 
@@ -363,7 +399,7 @@ int oracle_quantize(int mode, const void* x, int dtype, int64_t M, int64_t N,
         if (v > a) a = v;
       }
       float g = oracle_global_encode_scale(a);
-      quantize_vector_1d(vec, N, g, row_data + k * (N / 2), row_scale + k * (N / 16));
+      quantize_vector_1d(vec, N, g, NULL, 0, row_data + k * (N / 2), row_scale + k * (N / 16));
       if (amax_row_out) amax_row_out[k] = a;
     }
     free(vec);
@@ -397,14 +433,16 @@ int oracle_quantize(int mode, const void* x, int dtype, int64_t M, int64_t N,
       int64_t y0 = (y / 16) * 16;
       for (int64_t dy = 0; dy < 16; ++dy)
         for (int64_t j = 0; j < N; ++j) band[dy * N + j] = load_elem(x, dtype, (y0 + dy) * N + j);
-      quantize_row_2d(band, N, y - y0, g_row, row_data + k * (N / 2), row_scale + k * (N / 16));
+      quantize_row_2d(band, N, y - y0, g_row, rbits ? rbits + y * N : NULL, 1, row_data + k * (N / 2),
+                      row_scale + k * (N / 16));
     }
     free(band);
   } else {
     for (int64_t k = 0; k < nr; ++k) {
       int64_t y = row_ids ? row_ids[k] : k;
       for (int64_t j = 0; j < N; ++j) vec[j] = load_elem(x, dtype, y * N + j);
-      quantize_vector_1d(vec, N, g_row, row_data + k * (N / 2), row_scale + k * (N / 16));
+      quantize_vector_1d(vec, N, g_row, rbits ? rbits + y * N : NULL, 1, row_data + k * (N / 2),
+                         row_scale + k * (N / 16));
     }
   }
 
@@ -418,7 +456,8 @@ int oracle_quantize(int mode, const void* x, int dtype, int64_t M, int64_t N,
       int64_t j = col_ids ? col_ids[k] : k;
       int64_t j0 = (j / 16) * 16;
       for (int64_t dj = 0; dj < 16; ++dj) load_column(x, dtype, M, N, j0 + dj, band + dj * M);
-      quantize_row_2d(band, M, j - j0, g_col, col_data + k * (M / 2), col_scale + k * (M / 16));
+      quantize_row_2d(band, M, j - j0, g_col, rbits ? rbits + j : NULL, N, col_data + k * (M / 2),
+                      col_scale + k * (M / 16));
     }
     free(band);
   } else {
@@ -428,11 +467,39 @@ int oracle_quantize(int mode, const void* x, int dtype, int64_t M, int64_t N,
         load_rht_column(x, dtype, M, N, j, sign_mask, vec);
       else
         load_column(x, dtype, M, N, j, vec);
-      quantize_vector_1d(vec, M, g_col, col_data + k * (M / 2), col_scale + k * (M / 16));
+      quantize_vector_1d(vec, M, g_col, rbits ? rbits + j : NULL, N, col_data + k * (M / 2),
+                         col_scale + k * (M / 16));
     }
   }
   free(vec);
   return 0;
+}
+
+int oracle_quantize(int mode, const void* x, int dtype, int64_t M, int64_t N,
+                    int amax_given, float amax_row_in, float amax_col_in,
+                    uint32_t sign_mask,
+                    const int64_t* row_ids, int64_t n_row_ids,
+                    const int64_t* col_ids, int64_t n_col_ids,
+                    uint8_t* row_data, uint8_t* row_scale, float* amax_row_out,
+                    uint8_t* col_data, uint8_t* col_scale, float* amax_col_out) {
+  return quantize_impl(mode, x, dtype, M, N, amax_given, amax_row_in, amax_col_in, sign_mask, NULL, row_ids,
+                       n_row_ids, col_ids, n_col_ids, row_data, row_scale, amax_row_out, col_data, col_scale,
+                       amax_col_out);
+}
+
+/* oracle_quantize with stochastically rounded codes (MODE_1D or MODE_2D):
+ * rbits holds one random byte per element of x (M x N, row-major); element
+ * (y, j) uses rbits[y * N + j] in the row-wise and in the column-wise
+ * output. */
+int oracle_quantize_sr(int mode, const void* x, int dtype, int64_t M, int64_t N,
+                       int amax_given, float amax_row_in, float amax_col_in, const uint8_t* rbits,
+                       const int64_t* row_ids, int64_t n_row_ids,
+                       const int64_t* col_ids, int64_t n_col_ids,
+                       uint8_t* row_data, uint8_t* row_scale, float* amax_row_out,
+                       uint8_t* col_data, uint8_t* col_scale, float* amax_col_out) {
+  if (rbits == NULL && M > 0 && N > 0) return -1;
+  return quantize_impl(mode, x, dtype, M, N, amax_given, amax_row_in, amax_col_in, 0, rbits, row_ids, n_row_ids,
+                       col_ids, n_col_ids, row_data, row_scale, amax_row_out, col_data, col_scale, amax_col_out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -492,6 +559,10 @@ int oracle_dequantize(const uint8_t* data, const uint8_t* scale, const float* am
 
 void oracle_e2m1_array(const float* in, uint8_t* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_rn_satfinite(in[i]);
+}
+
+void oracle_e2m1_sr_array(const float* in, const uint8_t* rb, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_sr_satfinite(in[i], rb[i]);
 }
 
 void oracle_e4m3_array(const float* in, uint8_t* out, int64_t n) {

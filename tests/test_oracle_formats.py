@@ -76,6 +76,70 @@ def test_e2m1_boundaries_fp32_vs_rint(oracle_mod):
 # E4M3
 # ---------------------------------------------------------------------------
 
+# ---------------------------------------------------------------------------
+# E2M1 with stochastic rounding (one random byte per element)
+# ---------------------------------------------------------------------------
+
+E2M1_GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_sr_representable_values_never_move(oracle_mod):
+    for c in range(16):
+        v = oracle_mod.e2m1_value(c)
+        got = oracle_mod.e2m1_sr_array(np.full(256, v, np.float32), np.arange(256, dtype=np.uint8))
+        assert (got == c).all(), c
+
+
+def test_e2m1_sr_up_count_is_ceil_256f(oracle_mod):
+    """Over all 256 bytes, v between neighbours lo < v < hi rounds up for
+    exactly ceil(256 f) of them, f = (v - lo) / (hi - lo) as an exact
+    rational, and those are the smallest bytes (a threshold)."""
+    from fractions import Fraction
+    rb = np.arange(256, dtype=np.uint8)
+    for lo, hi in zip(E2M1_GRID[:-1], E2M1_GRID[1:]):
+        step = hi - lo
+        cands = [lo + step * k / 256 for k in (1, 37, 128, 255)] + \
+                [lo + step / 3, lo + step * 0.7071, np.nextafter(np.float32(lo), np.float32(7)),
+                 np.nextafter(np.float32(hi), np.float32(0))]
+        for v in np.array(cands, dtype=np.float32):
+            f = (Fraction(float(v)) - Fraction(lo)) / Fraction(step)
+            assert 0 < f < 1
+            want_up = math.ceil(f * 256)
+            got = oracle_mod.e2m1_sr_array(np.full(256, v, np.float32), rb)
+            lo_code, hi_code = E2M1_GRID.index(lo), E2M1_GRID.index(hi)
+            assert set(np.unique(got)) <= {lo_code, hi_code}
+            up = got == hi_code
+            assert int(up.sum()) == want_up, (float(v), lo, hi)
+            assert up[:want_up].all()                       # the smallest bytes round up
+
+
+def _e2m1_ceil(v: np.ndarray) -> np.ndarray:
+    """Independent: the smallest E2M1 magnitude >= |v| (numpy searchsorted),
+    saturated at 6, with the sign of v."""
+    m = np.minimum(np.abs(v.astype(np.float64)), 6.0)
+    code = np.searchsorted(np.array(E2M1_GRID), m, side="left").astype(np.uint8)
+    return code | np.where(np.signbit(v), 8, 0).astype(np.uint8)
+
+
+def test_e2m1_sr_zero_bytes_round_away_from_zero(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint32)
+    f = (bits << 16).view(np.float32)
+    f = f[np.isfinite(f)]
+    got = oracle_mod.e2m1_sr_array(f, np.zeros(f.size, np.uint8))
+    np.testing.assert_array_equal(got, _e2m1_ceil(f))
+
+
+def test_e2m1_sr_sign_and_saturation(oracle_mod):
+    rng = np.random.default_rng(3)
+    v = rng.uniform(0, 8, 4096).astype(np.float32)
+    rb = rng.integers(0, 256, 4096).astype(np.uint8)
+    pos = oracle_mod.e2m1_sr_array(v, rb)
+    neg = oracle_mod.e2m1_sr_array(-v, rb)
+    np.testing.assert_array_equal(neg, pos | 8)
+    assert (pos[v >= 6] == 7).all()
+    assert oracle_mod.e2m1_sr(-0.0, 0) == 8 and oracle_mod.e2m1_sr(float("inf"), 0) == 7
+
+
 def test_e4m3_golden_table(oracle_mod):
     for kind, a, b in _read("e4m3_values.txt"):
         if kind == "decode":

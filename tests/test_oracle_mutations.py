@@ -58,7 +58,7 @@ MUTANTS = {
     "tile_max_one_row": ("for (int dy = 0; dy < 16; ++dy)\n      for (int i = 0; i < 16; ++i) {",
                          "for (int dy = 0; dy < 1; ++dy)\n      for (int i = 0; i < 16; ++i) {"),
     # RHT: column-wise codes scaled by the row-wise (untransformed) amax
-    "rht_column_global_scale": ("quantize_vector_1d(vec, M, g_col, col_data", "quantize_vector_1d(vec, M, g_row, col_data"),
+    "rht_column_global_scale": ("quantize_vector_1d(vec, M, g_col, rbits", "quantize_vector_1d(vec, M, g_row, rbits"),
     # row-scaled: the tensor's amax instead of the row's
     "row_scaled_tensor_amax": ("float g = oracle_global_encode_scale(a);",
                                "float g = oracle_global_encode_scale(oracle_amax(x, dtype, M * N));"),
@@ -76,6 +76,16 @@ MUTANTS = {
                                "amax_col = amax_row;"),
     # swizzle: the two row terms of the 128x4 tile swapped
     "swizzle_row_terms": ("(r % 32) * 16 + ((r % 128) / 32) * 4", "(r % 32) * 4 + ((r % 128) / 32) * 16"),
+    # stochastic rounding: a byte equal to 256 f also rounds up
+    "sr_threshold_inclusive": ("int up = (double)rb < f * 256.0;", "int up = (double)rb <= f * 256.0;"),
+    # stochastic rounding: the sign of x dropped
+    "sr_sign_dropped": ("return (uint8_t)(sign | (uint8_t)(lo + up));", "return (uint8_t)(lo + up);"),
+    # stochastic rounding: the fraction measured in steps of 0.5 in every binade
+    "sr_fixed_step": ("double f = (m - E2M1_MAG[lo]) / (E2M1_MAG[lo + 1] - E2M1_MAG[lo]);",
+                      "double f = (m - E2M1_MAG[lo]) / 0.5;"),
+    # stochastic rounding: the column-wise output reads the bytes of x^T's layout
+    "sr_column_byte_index": ("quantize_vector_1d(vec, M, g_col, rbits ? rbits + j : NULL, N,",
+                             "quantize_vector_1d(vec, M, g_col, rbits ? rbits + j * M : NULL, 1,"),
 }
 
 

@@ -468,3 +468,116 @@ def test_grouped_rejects_bad_splits(oracle_mod):
         oracle_mod.quantize_grouped("1d", x, [16, 8])
     with pytest.raises(ValueError):
         oracle_mod.quantize_grouped("rht", x, [32])
+
+
+# ---------------------------------------------------------------------------
+# stochastic rounding of the codes (random bytes passed in)
+# ---------------------------------------------------------------------------
+
+def _rbits(M, N, seed):
+    return np.random.default_rng(seed).integers(0, 256, (M, N)).astype(np.uint8)
+
+
+def np_sr_codes(p, rb):
+    """Independent restatement of the stochastic rounding rule on arrays:
+    neighbours by searchsorted, f in float64 (exact), up iff rb < 256 f."""
+    m = np.abs(p.astype(np.float64))
+    sat = m >= 6.0
+    lo = np.clip(np.searchsorted(E2M1_GRID, m, side="right") - 1, 0, 6)
+    f = (m - E2M1_GRID[lo]) / (E2M1_GRID[lo + 1] - E2M1_GRID[lo])
+    code = np.where(sat, 7, lo + (rb.astype(np.float64) < 256.0 * f)).astype(np.uint8)
+    return code | np.where(np.signbit(p), 8, 0).astype(np.uint8)
+
+
+def np_sr_rows(X, b, g, rb):
+    g = np.asarray(g, np.float32).reshape(-1, 1)
+    s = np_e4m3((b / np.float32(6.0)) * g)
+    sv = np_e4m3_value(s)
+    with np.errstate(divide="ignore", over="ignore"):
+        r = np.where(s == 0, np.float32(0), np.minimum(g / sv, FLT_MAX)).astype(np.float32)
+    q = np_sr_codes(X * np.repeat(r, 16, axis=1), rb)
+    return (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8), s
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_sr_1d_matches_restatement(oracle_mod, dtype):
+    M, N = 48, 80
+    xt = inputs.outliers(M, N, seed=51, frac=0.02, dtype=dtype)
+    x = bits_any(xt)
+    X = to_f32(x)
+    rb = _rbits(M, N, 52)
+    out = oracle_mod.quantize("1d", x, rbits=rb)
+    g = np_global(np.abs(X).max())
+    b = np.abs(X).reshape(M, N // 16, 16).max(-1)
+    d, s = np_sr_rows(X, b, np.full(M, g, np.float32), rb)
+    np.testing.assert_array_equal(out["row_data"], d)
+    np.testing.assert_array_equal(out["row_scale"], s)
+    XT = np.ascontiguousarray(X.T)
+    bT = np.abs(XT).reshape(N, M // 16, 16).max(-1)
+    dT, sT = np_sr_rows(XT, bT, np.full(N, g, np.float32), np.ascontiguousarray(rb.T))
+    np.testing.assert_array_equal(out["col_data"], dT)
+    np.testing.assert_array_equal(out["col_scale"], sT)
+
+
+def bits_any(t):
+    return bf16_bits(t) if t.dtype == torch.bfloat16 else t.numpy()
+
+
+def test_sr_keeps_scales_and_amax(oracle_mod):
+    x = bf16_bits(inputs.randn(64, 96, seed=53))
+    for mode in ("1d", "2d"):
+        rn = oracle_mod.quantize(mode, x)
+        sr = oracle_mod.quantize(mode, x, rbits=_rbits(64, 96, 54))
+        for key in ("row_scale", "col_scale", "amax_row", "amax_col"):
+            np.testing.assert_array_equal(sr[key], rn[key])
+        assert (sr["row_data"] != rn["row_data"]).any()
+
+
+def test_sr_zero_bytes_round_every_product_away_from_zero(oracle_mod):
+    x = bf16_bits(inputs.randn(32, 64, seed=55))
+    X = to_f32(x)
+    out = oracle_mod.quantize("1d", x, colwise=False, rbits=np.zeros((32, 64), np.uint8))
+    g = np_global(np.abs(X).max())
+    b = np.abs(X).reshape(32, 4, 16).max(-1)
+    s = np_e4m3((b / np.float32(6.0)) * g)
+    r = np.where(s == 0, np.float32(0), g / np_e4m3_value(s)).astype(np.float32)
+    m = np.minimum(np.abs((X * np.repeat(r, 16, axis=1)).astype(np.float64)), 6.0)
+    q = np.searchsorted(E2M1_GRID, m, side="left").astype(np.uint8) | np.where(np.signbit(X), 8, 0).astype(np.uint8)
+    np.testing.assert_array_equal(out["row_data"], (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8))
+
+
+def test_sr_column_output_uses_the_elements_byte(oracle_mod):
+    """Column-wise output of x with bytes rb = row-wise output of x^T with
+    bytes rb^T: each element keeps its own random byte in both outputs."""
+    x = bf16_bits(inputs.randn(48, 64, seed=56))
+    rb = _rbits(48, 64, 57)
+    full = oracle_mod.quantize("1d", x, rbits=rb)
+    tr = oracle_mod.quantize("1d", np.ascontiguousarray(x.T), colwise=False, rbits=np.ascontiguousarray(rb.T))
+    np.testing.assert_array_equal(full["col_data"], tr["row_data"])
+
+
+def test_sr_2d_columns_are_the_transpose(oracle_mod):
+    M, N = 64, 96
+    x = bf16_bits(inputs.outliers(M, N, seed=58, frac=0.02))
+    out = oracle_mod.quantize("2d", x, rbits=_rbits(M, N, 59))
+    np.testing.assert_array_equal(out["col_data"], nibble_transpose(out["row_data"], M, N))
+
+
+def test_sr_is_unbiased_over_bytes(oracle_mod):
+    """Averaged over all 256 bytes, the decoded code of a product p is p to
+    within 1/256 of a step (P(up) = ceil(256 f) / 256)."""
+    x = np.array([[0.3, -1.1, 2.6, 4.9, 0.02, -5.5, 1.76, 3.14159] * 2], np.float32)
+    vals = []
+    for byte in range(256):
+        out = oracle_mod.quantize("1d", x, colwise=False, rbits=np.full(x.shape, byte, np.uint8))
+        q = np.empty(16, np.uint8)
+        q[0::2] = out["row_data"][0] & 0xF
+        q[1::2] = out["row_data"][0] >> 4
+        vals.append(np.where(q & 8, -1.0, 1.0) * E2M1_GRID[q & 7])
+    s = out["row_scale"][0, 0]
+    g = np_global(np.float32(np.abs(x).max()))
+    r = np.float32(g / np_e4m3_value(np.array([s]))[0])
+    p = (x[0] * r).astype(np.float64)
+    step = np.where(np.abs(p) < 2, 0.5, np.where(np.abs(p) < 4, 1.0, 2.0))
+    mean = np.mean(vals, axis=0)
+    assert np.all(np.abs(mean - p) <= step / 256 + 1e-12)
