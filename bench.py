@@ -386,6 +386,22 @@ def bench_variants(nv, inputs, args, dev, flush, stream):
                                       "frac": round(dbytes / (dms / 1e3) / 1e9 / peak, 4)}
         del x, q
         torch.cuda.empty_cache()
+    # stochastic rounding: inputs.SR with its random bytes (1 byte per
+    # element read on top of the plain quantize's traffic)
+    spec = inputs.SR
+    x = inputs.make(spec).to(dev)
+    rb = inputs.random_bytes(spec["M"], spec["N"], seed=spec["rbits_seed"]).to(dev)
+    q = nv.empty(spec["M"], spec["N"], swizzled=spec["swizzled"], device=dev)
+    sstep = lambda: nv.quantize_sr(x, rb, spec["mode"], swizzled=spec["swizzled"], out=q)  # noqa
+    for _ in range(3):
+        sstep()
+    sms = statistics.median(time_steps(sstep, steps, flush, stream))
+    sbytes = spec["M"] * spec["N"] * (BYTES_PER_ELEM[("bf16", "rowcol")] + 1.0)
+    out[f"sr_{spec['mode']}_{spec['M']}x{spec['N']}_bf16"] = {
+        "ms": round(sms, 5), "GB/s": round(sbytes / (sms / 1e3) / 1e9, 1),
+        "frac": round(sbytes / (sms / 1e3) / 1e9 / peak, 4)}
+    del x, rb, q
+    torch.cuda.empty_cache()
     # grouped quantize: the members of inputs.GROUPED (8192 x 5120 in all),
     # each with its own amax, in three launches
     spec = inputs.GROUPED

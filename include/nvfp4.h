@@ -152,6 +152,26 @@ nvfp4_status nvfp4_quantize_row_scaled(const void* x, int dtype, int64_t M, int6
                                        const float* noop, void* stream);
 
 /*
+ * 1D / 2D quantize with stochastically rounded codes ("Fuse NVFP4 scale
+ * swizzling on SM120 and SM121", Tests: stochastic rounding is one axis of
+ * the comparisons).  Amax, block scales, layouts and flags as
+ * nvfp4_quantize_1d / _2d; each product p = x * g / float(s) is rounded to
+ * one of its two neighbouring E2M1 magnitudes lo <= |p| < hi: to hi iff
+ * rbits[y * N + j] < 256 (|p| - lo) / (hi - lo) for element (y, j) of x, in
+ * the row-wise and in the column-wise output alike (|p| >= 6 saturates; the
+ * sign of x is kept).  With uniform random bytes P(hi) = ceil(256 f) / 256.
+ *   rbits: M x N bytes of device memory, row-major like x, 16-byte aligned,
+ *   owned by the caller (the random numbers are an input; the library draws
+ *   none).  N % 16 == 0; 2D also M % 16 == 0.
+ */
+nvfp4_status nvfp4_quantize_1d_sr(const void* x, int dtype, int64_t M, int64_t N,
+                                  const nvfp4_output* out, unsigned flags, const uint8_t* rbits,
+                                  const float* noop, void* stream);
+nvfp4_status nvfp4_quantize_2d_sr(const void* x, int dtype, int64_t M, int64_t N,
+                                  const nvfp4_output* out, unsigned flags, const uint8_t* rbits,
+                                  const float* noop, void* stream);
+
+/*
  * Grouped (multi-tensor) 1D / 2D quantize: x (row-major, N columns) stacks
  * num_groups member tensors along its first dimension, member g being the
  * group_rows[g] rows that follow the earlier members' rows.  Every member is

@@ -11,7 +11,9 @@ Hadamard transform, dequantize) runs in the library's CUDA kernels.
 Modes: "1d" (1x16 blocks), "2d" (16x16 tiles), "rht" (random Hadamard
 transform on the column-wise path) and "row_scaled" (one amax per row,
 row-wise only).  ``quantize_grouped`` quantizes several tensors stacked along
-the first dimension, each with its own amax, in three launches.
+the first dimension, each with its own amax, in three launches;
+``quantize_sr`` rounds the codes stochastically with caller-supplied random
+bytes.
 
 Paths for "1d" / "2d" / "rht": "single_pass" (one persistent kernel: amax,
 grid barrier, cast; x read from HBM once; needs a small workspace, which
@@ -39,7 +41,8 @@ FP32 = 1
 
 __all__ = ["NVFP4Tensor", "NVFP4Error", "empty", "compute_amax", "compute_amax_rht", "quantize",
            "single_pass_workspace", "reset_workspaces",
-           "quantize_1d", "quantize_2d", "quantize_rht", "quantize_row_scaled", "quantize_grouped", "dequantize",
+           "quantize_1d", "quantize_2d", "quantize_rht", "quantize_row_scaled", "quantize_grouped", "quantize_sr",
+           "dequantize",
            "swizzle_scales", "scale_bytes", "device_status"]
 
 
@@ -231,6 +234,38 @@ def quantize(x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: b
         else:
             raise ValueError(f"unknown mode {mode!r}")
     _lib.check(rc, f"nvfp4 quantize ({mode})")
+    return out
+
+
+def quantize_sr(x: torch.Tensor, rbits: torch.Tensor, mode: str = "1d", rowwise: bool = True,
+                colwise: bool = True, swizzled: bool = False, out: NVFP4Tensor | None = None,
+                skip_amax: bool = False, noop: torch.Tensor | None = None) -> NVFP4Tensor:
+    """NVFP4 quantize (mode "1d" or "2d") with stochastically rounded codes.
+
+    rbits: a uint8 CUDA tensor of x's shape, the random numbers (the library
+    draws none): element (y, j) of x rounds to the upper neighbouring E2M1
+    magnitude iff rbits[y, j] < 256 f, f its position between the two, in
+    both outputs.  Scales, amax and layouts as ``quantize``."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (M x N)")
+    if mode not in ("1d", "2d"):
+        raise ValueError("stochastic rounding: mode '1d' or '2d'")
+    if rbits.dtype != torch.uint8 or tuple(rbits.shape) != tuple(x.shape):
+        raise ValueError("rbits must be a uint8 tensor of x's shape")
+    M, N = x.shape
+    if out is None:
+        out = empty(M, N, rowwise, colwise, swizzled=swizzled, device=x.device)
+    out.swizzled = swizzled
+    _require_cuda(x, rbits, out.data_row, out.scale_row, out.amax_row, out.data_col, out.scale_col, out.amax_col,
+                  noop)
+    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLED if swizzled else 0) | \
+        (SKIP_AMAX if skip_amax else 0)
+    L = _lib.load()
+    st = out.c_struct()
+    fn = L.nvfp4_quantize_1d_sr if mode == "1d" else L.nvfp4_quantize_2d_sr
+    with _OnDevice(x.device):
+        rc = fn(_ptr(x), _dtype_code(x), M, N, ctypes.byref(st), flags, _ptr(rbits), _ptr(noop), _stream(x.device))
+    _lib.check(rc, f"nvfp4 stochastic-rounding quantize ({mode})")
     return out
 
 

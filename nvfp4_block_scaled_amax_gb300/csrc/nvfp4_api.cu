@@ -9,6 +9,7 @@
 #include "grouped.h"
 #include "kernels.h"
 #include "nvfp4.h"
+#include "sr.h"
 
 // Per-device status word of bounded device-side waits.
 __device__ unsigned int g_nvfp4_status_word;
@@ -188,6 +189,45 @@ nvfp4_status quantize_single_pass(int mode, const void* x, int dtype, int64_t M,
   a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
   return from_cuda(launch_single_pass(x, dtype == NVFP4_BF16, mode, a,
                                       static_cast<SinglePassWorkspace*>(workspace), ctx));
+}
+
+// Quantize with stochastically rounded codes: the checks of the plain
+// quantize, plus the random bytes (one per element of x, 16-byte aligned).
+nvfp4_status quantize_sr(int mode, const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,
+                         unsigned flags, const uint8_t* rbits, const float* noop, void* stream) {
+  const unsigned allowed = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SWIZZLED | NVFP4_SKIP_AMAX;
+  nvfp4_status st = check_quantize(x, dtype, M, N, out, flags, allowed);
+  if (st != NVFP4_OK) return st;
+  if (N % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (mode == kCast2D && M % 16 != 0) return NVFP4_ERR_SHAPE;
+  if (M > 0 && N > 0 && rbits == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(rbits)) return NVFP4_ERR_ALIGN;
+  if (noop != nullptr && !aligned16(noop)) return NVFP4_ERR_ALIGN;
+  LaunchCtx ctx;
+  if ((st = make_ctx(stream, &ctx)) != NVFP4_OK) return st;
+  const bool row = flags & NVFP4_ROWWISE, col = flags & NVFP4_COLWISE;
+  float* a_row = row ? out->amax_row : nullptr;
+  float* a_col = col ? out->amax_col : nullptr;
+  const bool skip = flags & NVFP4_SKIP_AMAX;
+  if (!skip && launch_amax(x, dtype == NVFP4_BF16, M * N, a_row ? a_row : a_col, a_row ? a_col : nullptr, noop,
+                           ctx) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  if (M == 0 || N == 0) return NVFP4_OK;
+  CastArgs a = {};
+  a.M = M;
+  a.N = N;
+  a.data_row = row ? out->data_row : nullptr;
+  a.scale_row = row ? out->scale_row : nullptr;
+  a.amax_row = a_row;
+  a.data_col = col ? out->data_col : nullptr;
+  a.scale_col = col ? out->scale_col : nullptr;
+  a.amax_col = a_col;
+  a.noop = noop;
+  a.status = ctx.status;
+  a.rowwise = row;
+  a.colwise = col;
+  a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
+  return from_cuda(launch_cast_sr(x, dtype == NVFP4_BF16, mode, a, rbits, /*pdl=*/!skip, ctx));
 }
 
 static_assert(NVFP4_MAX_GROUPS == kMaxGroups, "member table size");
@@ -421,6 +461,16 @@ nvfp4_status nvfp4_quantize_row_scaled(const void* x, int dtype, int64_t M, int6
   }
   return from_cuda(launch_row_scaled(x, dtype == NVFP4_BF16, M, N, out->data_row, out->scale_row, out->amax_row,
                                      (flags & NVFP4_SKIP_AMAX) != 0, (flags & NVFP4_SWIZZLED) != 0, noop, ctx));
+}
+
+nvfp4_status nvfp4_quantize_1d_sr(const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,
+                                  unsigned flags, const uint8_t* rbits, const float* noop, void* stream) {
+  return quantize_sr(kCast1D, x, dtype, M, N, out, flags, rbits, noop, stream);
+}
+
+nvfp4_status nvfp4_quantize_2d_sr(const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,
+                                  unsigned flags, const uint8_t* rbits, const float* noop, void* stream) {
+  return quantize_sr(kCast2D, x, dtype, M, N, out, flags, rbits, noop, stream);
 }
 
 nvfp4_status nvfp4_quantize_grouped_1d(const void* x, int dtype, int64_t N, int num_groups,

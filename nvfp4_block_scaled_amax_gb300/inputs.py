@@ -106,6 +106,17 @@ WORKLOADS = {
 }
 
 
+def random_bytes(M: int, N: int, seed: int) -> torch.Tensor:
+    """Uniform random bytes (uint8, M x N): the random numbers of
+    stochastic rounding, drawn on the host."""
+    return torch.randint(0, 256, (M, N), generator=_gen(seed), dtype=torch.int32).to(torch.uint8)
+
+
+# Stochastic rounding: the 1D 8192x5120 BF16 workload (seed 6) with random
+# bytes drawn from seed 9.
+SR = dict(mode="1d", M=8192, N=5120, dtype=torch.bfloat16, gen="randn", seed=6, swizzled=True, rbits_seed=9)
+
+
 # Grouped quantize (tensors stacked along the first dimension, each with its
 # own amax): eight members of uneven height, multiples of 128, 8192 rows in
 # all, N = 5120; member g is N(0, 1) times 10^e_g, e_g drawn from the seed in

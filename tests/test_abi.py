@@ -59,7 +59,10 @@ def test_scale_bytes(lib):
     assert lib.nvfp4_scale_bytes(256, 32, 0, None) == ERR_NULL
 
 
-# fake, 16-byte aligned device addresses: validation never dereferences them
+# Fake, 16-byte aligned device addresses: validation never dereferences them.
+# Every call in this file must FAIL validation: one that passed would launch
+# kernels on these addresses on a machine with a GPU (valid argument sets are
+# exercised by the GPU tests, on real buffers).
 X, A, B, C, D, E, F, NOOP = (0x100000 * (i + 1) for i in range(8))
 
 
@@ -134,6 +137,19 @@ def test_amax_and_misc_validation(lib):
     assert lib.nvfp4_device_status(None, 0) == ERR_NULL
 
 
+def test_sr_validation(lib):
+    o = out(lib)
+    for fn in (lib.nvfp4_quantize_1d_sr, lib.nvfp4_quantize_2d_sr):
+        assert fn(X, 0, 256, 256, ctypes.byref(o), ROW | COL, None, None, None) == ERR_NULL     # random bytes
+        assert fn(X, 0, 256, 256, ctypes.byref(o), ROW | COL, A + 8, None, None) == ERR_ALIGN
+        assert fn(X, 0, 256, 256, ctypes.byref(o), ROW | ROWSC, A, None, None) == ERR_FLAGS
+        assert fn(X, 2, 256, 256, ctypes.byref(o), ROW, A, None, None) == ERR_DTYPE
+        assert fn(X, 0, 256, 24, ctypes.byref(o), COL, A, None, None) == ERR_SHAPE            # N % 16 always
+        assert fn(X, 0, 192, 256, ctypes.byref(o), ROW | SWZ, A, None, None) == ERR_ALIGN
+        assert fn(X, 0, 256, 256, None, ROW, A, None, None) == ERR_NULL
+    assert lib.nvfp4_quantize_2d_sr(X, 0, 24, 256, ctypes.byref(o), ROW, A, None, None) == ERR_SHAPE
+
+
 def test_grouped_validation(lib):
     from nvfp4_block_scaled_amax_gb300._lib import Output
 
@@ -161,7 +177,6 @@ def test_grouped_validation(lib):
     assert grouped([128] * 65) == ERR_SHAPE                          # at most 64
     assert grouped([128, -16]) == ERR_SHAPE
     assert grouped([128, 24]) == ERR_SHAPE                           # column blocks need rows % 16
-    assert grouped([128, 24], flags=ROW) != ERR_SHAPE                # row-wise 1D does not
     assert grouped([128, 24], flags=ROW, fn=lib.nvfp4_quantize_grouped_2d) == ERR_SHAPE
     assert grouped([128], N=24, flags=ROW) == ERR_SHAPE
     assert grouped([128], dtype=2) == ERR_DTYPE
@@ -170,7 +185,6 @@ def test_grouped_validation(lib):
     assert grouped([128, 64], flags=ROW | COL | SWZ) == ERR_ALIGN     # swizzle needs 128-row members
     assert grouped([128], x=X + 8) == ERR_ALIGN
     assert grouped([128], x=0) == ERR_NULL
-    assert grouped([0], x=0) != ERR_NULL                             # an empty member reads nothing
     assert grouped([128, 128], o=members(2, {1: dict(scale_col=0)})) == ERR_NULL
     assert grouped([128, 128], o=members(2, {1: dict(data_row=0x7)})) == ERR_ALIGN
     shared = members(2, {1: dict(amax_row=0x1000000 + 0x200000)})  # member 1 reuses member 0's amax
