@@ -10,15 +10,44 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "nvfp4.h")
 
-OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_FLAGS = 0, 1, 2, 3, 4, 5
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_FLAGS, ERR_CUDA = 0, 1, 2, 3, 4, 5, 6
 ROW, COL, SWZ, SKIP, ROWSC = 1, 2, 4, 8, 16
+
+# The calls below pass fake device addresses, so they must never reach a
+# launch: the module does not run where a GPU is visible, and on a machine
+# without one the fixture fails any call that got past validation (it then
+# stops at the CUDA context, NVFP4_ERR_CUDA).
+pytestmark = pytest.mark.skipif(
+    __import__("torch").cuda.is_available(),
+    reason="validation-only tests with fake device addresses: run on a machine without a GPU")
+
+HOST_ONLY = ("nvfp4_status_string", "nvfp4_scale_bytes")
+
+
+class _ValidationOnly:
+    """The library, with every device entry point checked to fail validation."""
+
+    def __init__(self, lib):
+        self._lib = lib
+
+    def __getattr__(self, name):
+        fn = getattr(self._lib, name)
+        if not name.startswith("nvfp4_") or name in HOST_ONLY:
+            return fn
+
+        def call(*args):
+            rc = fn(*args)
+            if rc == ERR_CUDA:
+                pytest.fail(f"{name} accepted fake device addresses (it would launch on a GPU machine)")
+            return rc
+        return call
 
 
 @pytest.fixture(scope="module")
 def lib():
     from nvfp4_block_scaled_amax_gb300 import _lib, build
     build.build()
-    return _lib.load()
+    return _ValidationOnly(_lib.load())
 
 
 def declared_functions():
