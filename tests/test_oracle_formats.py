@@ -83,6 +83,12 @@ def test_e2m1_boundaries_fp32_vs_rint(oracle_mod):
 E2M1_GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
 
 
+def test_e2m1_sr_golden_table(oracle_mod):
+    for line in _read("e2m1_sr.txt"):
+        v, byte, code = float(line[0]), int(line[1]), int(line[2])
+        assert oracle_mod.e2m1_sr(v, byte) == code, (v, byte)
+
+
 def test_e2m1_sr_representable_values_never_move(oracle_mod):
     for c in range(16):
         v = oracle_mod.e2m1_value(c)
