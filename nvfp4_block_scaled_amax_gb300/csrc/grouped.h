@@ -1,7 +1,7 @@
 // grouped.h -- grouped (multi-tensor) quantize: the member table the three
 // kernels of grouped.cu share, passed by value as a kernel parameter (no
-// device-side table, so a call allocates nothing and can be captured in a
-// CUDA graph).
+// device-side table: a call allocates nothing and its launches carry all of
+// its state).
 #pragma once
 
 #include "kernels.h"
