@@ -9,7 +9,8 @@ reduction that follows the local one, "Write both NVFP4 amax buffers",
 Description), and every rank then casts its slab with the agreed amax
 (SKIP_AMAX).  With RHT the vector carries the row amax and the amax after
 the transform.  Row-scaled rows are independent tensors, so that mode needs
-no exchange.
+no exchange.  With stochastic rounding each rank passes the rows of the
+random bytes that match its slab, so every element keeps its byte.
 
 A rank's row-wise output is rows [start, stop) of the full row-wise output;
 its column-wise output is columns [start/2, stop/2) of the packed codes of
@@ -28,7 +29,7 @@ from typing import Callable, Sequence
 
 import torch
 
-from . import NVFP4Tensor, compute_amax, compute_amax_rht, empty, quantize
+from . import NVFP4Tensor, compute_amax, compute_amax_rht, empty, quantize, quantize_sr
 
 __all__ = ["ShardError", "slab_bounds", "slab_alignment", "check_slab", "CudaBackend", "quantize_slab",
            "assemble", "all_reduce_max"]
@@ -102,13 +103,16 @@ class CudaBackend:
         return a[0::4]
 
     def cast(self, x: torch.Tensor, mode: str, amax: torch.Tensor, rowwise: bool, colwise: bool,
-             swizzled: bool, sign_mask: int) -> NVFP4Tensor:
+             swizzled: bool, sign_mask: int, rbits: torch.Tensor | None = None) -> NVFP4Tensor:
         M, N = x.shape
         out = empty(M, N, rowwise, colwise, swizzled=swizzled, device=x.device)
         if out.amax_row is not None:
             out.amax_row.copy_(amax[0:1])
         if out.amax_col is not None:
             out.amax_col.copy_(amax[1:2])
+        if rbits is not None:
+            return quantize_sr(x, rbits, mode, rowwise=rowwise, colwise=colwise, swizzled=swizzled, out=out,
+                               skip_amax=True)
         return quantize(x, mode, rowwise=rowwise, colwise=colwise, swizzled=swizzled, sign_mask=sign_mask,
                         out=out, skip_amax=True)
 
@@ -118,11 +122,13 @@ class CudaBackend:
 
 def quantize_slab(x_local: torch.Tensor, mode: str = "1d", *, rowwise: bool = True, colwise: bool = True,
                   swizzled: bool = False, sign_mask: int = 0, group=None, backend=None,
-                  exchange: Callable[[torch.Tensor], torch.Tensor] | None = None) -> NVFP4Tensor:
+                  exchange: Callable[[torch.Tensor], torch.Tensor] | None = None,
+                  rbits_local: torch.Tensor | None = None) -> NVFP4Tensor:
     """Quantizes this rank's row slab of a tensor split over the ranks.
 
     Every rank of the group calls this with its slab (the same N, mode and
-    flags).  `exchange` replaces the MAX all-reduce over `group` (it gets
+    flags).  `rbits_local`: stochastic rounding of the codes (modes 1d and
+    2d), the rows of the random bytes that match the slab.  `exchange` replaces the MAX all-reduce over `group` (it gets
     and returns the float32 vector [error, amax_row, amax_col]); `backend`
     replaces the library's kernels.  Raises ShardError on every rank when
     any rank's slab fails its local step."""
@@ -131,6 +137,8 @@ def quantize_slab(x_local: torch.Tensor, mode: str = "1d", *, rowwise: bool = Tr
     if x_local.dim() != 2:
         raise ValueError("x_local must be 2-D")
     M_local, N = x_local.shape
+    if rbits_local is not None and (mode not in ("1d", "2d") or tuple(rbits_local.shape) != (M_local, N)):
+        raise ValueError("rbits_local: modes 1d / 2d, one byte per element of the slab")
     if mode == "row_scaled":
         check_slab(M_local, N, mode, rowwise, False, swizzled)
         return backend.quantize_rows(x_local, swizzled)
@@ -148,6 +156,8 @@ def quantize_slab(x_local: torch.Tensor, mode: str = "1d", *, rowwise: bool = Tr
     vals = exchange(vals)
     if float(vals[0]) != 0.0:
         raise ShardError(f"this rank's slab failed ({why})" if why else "another rank's slab failed")
+    if rbits_local is not None:
+        return backend.cast(x_local, mode, vals[1:3], rowwise, colwise, swizzled, sign_mask, rbits=rbits_local)
     return backend.cast(x_local, mode, vals[1:3], rowwise, colwise, swizzled, sign_mask)
 
 

@@ -95,10 +95,11 @@ class OracleBackend:
         a = oracle.amax(xb)
         return torch.tensor([a, oracle.rht_amax(xb, sign_mask) if mode == "rht" else a], dtype=torch.float32)
 
-    def cast(self, x, mode, amax, rowwise, colwise, swizzled, sign_mask):
+    def cast(self, x, mode, amax, rowwise, colwise, swizzled, sign_mask, rbits=None):
         import oracle
         d = oracle.quantize(mode, _bits(x), rowwise, colwise, sign_mask=sign_mask,
-                            amax=(float(amax[0]), float(amax[1])))
+                            amax=(float(amax[0]), float(amax[1])),
+                            rbits=None if rbits is None else rbits.contiguous().numpy())
         return _to_tensor(d, x.shape[0], x.shape[1], swizzled, False, rowwise, colwise)
 
     def quantize_rows(self, x, swizzled):
@@ -116,6 +117,7 @@ def _free_port() -> int:
 
 
 CASES = [("1d", False), ("1d", True), ("2d", True), ("rht", False), ("row_scaled", True), ("row_scaled", False)]
+SR_CASES = [("1d", True), ("2d", False)]
 
 
 def _make_input(mode: str, M: int, N: int) -> torch.Tensor:
@@ -141,6 +143,15 @@ def _rank_main(rank, world, port, outdir, scenario):
                 results[(mode, swz)] = {k: (None if getattr(q, k) is None else getattr(q, k).numpy())
                                         for k in ("data_row", "scale_row", "amax_row", "data_col", "scale_col",
                                                   "amax_col")} | {"M": q.M}
+            rb = inputs.random_bytes(M, N, seed=64)
+            for mode, swz in SR_CASES:
+                x = _make_input(mode, M, N)
+                a, b = slab_bounds(M, world, rank, slab_alignment(mode, True, swz))
+                q = quantize_slab(x[a:b].contiguous(), mode, swizzled=swz, backend=OracleBackend(),
+                                  rbits_local=rb[a:b].contiguous())
+                results[("sr", mode, swz)] = {k: getattr(q, k).numpy() for k in
+                                              ("data_row", "scale_row", "amax_row", "data_col", "scale_col",
+                                               "amax_col")} | {"M": q.M}
         elif scenario == "bad_slab":
             x = inputs.randn(64, 64, seed=5)
             part = x[:40] if rank == 1 else x[:32]  # rank 1: 40 rows, not a multiple of 16
@@ -209,6 +220,31 @@ def test_gloo_two_ranks_match_one_call_on_the_whole_tensor(tmp_path, oracle_mod)
             assert (e is None) == (g is None), (mode, swz, k)
             if e is not None:
                 np.testing.assert_array_equal(g.numpy(), e.numpy(), err_msg=f"{mode} swizzled={swz} {k}")
+
+
+def test_gloo_two_ranks_stochastic_rounding_matches_one_call(tmp_path, oracle_mod):
+    """Each rank rounds its slab with the matching rows of the random bytes:
+    the assembled result is the whole tensor's stochastic rounding."""
+    parts = _spawn("parity", tmp_path)
+    M, N = 384, 256
+    rb = inputs.random_bytes(M, N, seed=64)
+    for mode, swz in SR_CASES:
+        pieces = []
+        for r in range(2):
+            d = parts[r][("sr", mode, swz)]
+            q = NVFP4Tensor(d["M"], N, swizzled=swz)
+            for k in ("data_row", "scale_row", "amax_row", "data_col", "scale_col", "amax_col"):
+                setattr(q, k, torch.from_numpy(d[k]))
+            pieces.append(q)
+        whole = assemble(pieces)
+        x = _make_input(mode, M, N)
+        ref = OracleBackend()
+        exp = ref.cast(x, mode, ref.local_amax(x, mode, 0), True, True, swz, 0, rbits=rb)
+        for k in ("data_row", "scale_row", "amax_row", "data_col", "scale_col", "amax_col"):
+            np.testing.assert_array_equal(getattr(whole, k).numpy(), getattr(exp, k).numpy(),
+                                          err_msg=f"sr {mode} swizzled={swz} {k}")
+        assert not np.array_equal(exp.data_row.numpy(), ref.cast(x, mode, ref.local_amax(x, mode, 0), True, True,
+                                                                  swz, 0).data_row.numpy())
 
 
 def test_gloo_invalid_slab_raises_on_every_rank(tmp_path):
