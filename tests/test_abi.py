@@ -63,6 +63,20 @@ def test_header_declares_the_boundary():
         assert required in names
 
 
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++17")])
+def test_header_compiles_for_c_and_cpp_hosts(tmp_path, lang, std):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    src.write_text('#include "nvfp4.h"\nint main(void) { nvfp4_output o; (void)o; '
+                   'return (int)NVFP4_MAX_GROUPS - 64; }\n')
+    subprocess.check_call([cc, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                           "-I", os.path.join(ROOT, "include"), str(src)])
+
+
 def test_library_exports_every_declared_function(lib):
     from nvfp4_block_scaled_amax_gb300 import _lib
     names = declared_functions()
