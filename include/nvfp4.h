@@ -29,10 +29,17 @@
  *     Device pointers must be 16-byte aligned (NVFP4_ERR_ALIGN otherwise).
  *   * stream is a cudaStream_t (NULL = the legacy default stream).  All work
  *     is enqueued on it asynchronously; no call synchronizes the device.
- *   * Arguments are validated on the host before anything is enqueued: a
- *     non-OK status means nothing was launched and no output was written.
- *     NVFP4_ERR_CUDA means a launch failed (the CUDA error is sticky in the
- *     calling thread's runtime, cudaGetLastError() reads it).
+ *   * Arguments are validated, and the tensor map through which the kernels
+ *     read x is encoded, on the host before anything is enqueued: every
+ *     status but NVFP4_ERR_CUDA means nothing was launched and no output was
+ *     written.  NVFP4_ERR_CUDA means a CUDA call failed (cudaGetLastError()
+ *     reads the error): if it was the launch of a call's second kernel, the
+ *     first one (the amax reduction ahead of a cast) was enqueued and may
+ *     still write the amax buffers.
+ *   * Quantize shapes: N % 16 == 0 always (row-wise blocks span 16 columns,
+ *     and x is staged through a tensor map whose row pitch must be a multiple
+ *     of 16 bytes); with COLWISE, or for 2D / RHT, also M % 16 == 0; row-wise
+ *     output alone takes any M >= 0.
  *   * noop: NULL, or a device float; when it holds 1.0f at execution time the
  *     call writes nothing at all, amax buffers included ("Write both NVFP4
  *     amax buffers", Changes: with a noop flag set both buffers are left
@@ -54,11 +61,11 @@ extern "C" {
 typedef enum {
   NVFP4_OK = 0,
   NVFP4_ERR_NULL = 1,    /* a required pointer is NULL                        */
-  NVFP4_ERR_SHAPE = 2,   /* negative size, or a blocked dimension not % 16     */
+  NVFP4_ERR_SHAPE = 2,   /* negative size, or a dimension not % 16 (above)     */
   NVFP4_ERR_ALIGN = 3,   /* SWIZZLED on a shape not 128-aligned; bad pointer   */
   NVFP4_ERR_DTYPE = 4,   /* unknown dtype, or one the operation does not take  */
   NVFP4_ERR_FLAGS = 5,   /* unknown / contradictory flags; aliased amax buffers */
-  NVFP4_ERR_CUDA = 6,    /* a kernel launch failed                             */
+  NVFP4_ERR_CUDA = 6,    /* a CUDA call failed (see the conventions above)     */
   NVFP4_ERR_TIMEOUT = 7  /* a device-side wait ran out (nvfp4_device_status)   */
 } nvfp4_status;
 
@@ -119,7 +126,7 @@ nvfp4_status nvfp4_compute_amax_rht(const void* x, int dtype, int64_t M, int64_t
  * or swizzled ("Write both NVFP4 amax buffers"; "Fuse NVFP4 scale swizzling
  * on SM120 and SM121", Changes: the generic and tuned 1D kernels gain a
  * swizzled store).  flags: ROWWISE | COLWISE (at least one) | SWIZZLED |
- * SKIP_AMAX.  ROWWISE needs N % 16 == 0, COLWISE needs M % 16 == 0.
+ * SKIP_AMAX.  N % 16 == 0; COLWISE also needs M % 16 == 0.
  * Both amax buffers receive max|x|; with SKIP_AMAX the kernel reads them
  * instead (e.g. after a cross-rank MAX) and writes none.
  */
@@ -270,7 +277,10 @@ nvfp4_status nvfp4_quantize_rht_single_pass(const void* x, int dtype, int64_t M,
  * cudaFree, and processes that size all device memory up front.
  *   * The first call on a device looks up the array's device address (a
  *     runtime query, no allocation); make that first call before any stream
- *     capture on that device.
+ *     capture on that device.  The address is kept for the life of the
+ *     process: it belongs to the device's primary context, so after
+ *     cudaDeviceReset() on a device this entry point must not be called on
+ *     that device again (the kept address would be stale).
  *   * Every call clears the array's 64-byte barrier header on `stream` (a
  *     memset) and then launches the kernel; it calls no cudaMalloc /
  *     cudaFree.

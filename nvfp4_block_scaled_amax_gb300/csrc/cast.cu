@@ -239,14 +239,7 @@ cudaError_t launch_t(const CUtensorMap& map, const CastArgs& a, bool pdl, const 
 
 }  // namespace
 
-// Tensor map of x: dims {N, M}, box {128 bytes, 128 rows}, 128-byte swizzle,
-// zero fill outside the tensor.
-cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N);
-
-cudaError_t launch_cast(const void* x, bool bf16, int mode, CastArgs args, bool pdl, const LaunchCtx& ctx) {
-  CUtensorMap map;
-  cudaError_t e = make_x_tensor_map(&map, x, bf16, args.M, args.N);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_cast(const CUtensorMap& map, bool bf16, int mode, CastArgs args, bool pdl, const LaunchCtx& ctx) {
   const int64_t tiles_m = (args.M + kTile - 1) / kTile, tiles_n = (args.N + kTile - 1) / kTile;
   args.tiles_n = (int)tiles_n;
   args.num_tiles = (int)(tiles_m * tiles_n);

@@ -360,18 +360,13 @@ cudaError_t launch_fused_t(const CUtensorMap& map, const CastArgs& a, SinglePass
 
 }  // namespace
 
-cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N);
-
 int single_pass_grid(int64_t M, int64_t N, const LaunchCtx& ctx) {
   const int64_t tiles = ((M + kTile - 1) / kTile) * ((N + kTile - 1) / kTile);
   return (int)(tiles < ctx.num_sms ? tiles : ctx.num_sms);
 }
 
-cudaError_t launch_single_pass(const void* x, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
+cudaError_t launch_single_pass(const CUtensorMap& map, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
                                const LaunchCtx& ctx) {
-  CUtensorMap map;
-  cudaError_t e = make_x_tensor_map(&map, x, bf16, args.M, args.N);
-  if (e != cudaSuccess) return e;
   const int64_t tiles_m = (args.M + kTile - 1) / kTile, tiles_n = (args.N + kTile - 1) / kTile;
   args.tiles_n = (int)tiles_n;
   args.num_tiles = (int)(tiles_m * tiles_n);

@@ -315,10 +315,8 @@ cudaError_t launch_cast_t(const CUtensorMap& map, const GroupedArgs& ga, bool pd
 
 }  // namespace
 
-cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N);
-
-cudaError_t launch_grouped(const void* x, bool bf16, int mode, int64_t total_rows, GroupedArgs ga, bool skip_amax,
-                           const LaunchCtx& ctx) {
+cudaError_t launch_grouped(const void* x, const CUtensorMap* map, bool bf16, int mode, GroupedArgs ga,
+                           bool skip_amax, const LaunchCtx& ctx) {
   const int epv = bf16 ? 8 : 4;
   ga.tiles_n = (int)((ga.N + kTile - 1) / kTile);
   ga.tile_start[0] = 0;
@@ -349,16 +347,14 @@ cudaError_t launch_grouped(const void* x, bool bf16, int mode, int64_t total_row
       if ((e = launch_pdl(fn, dim3(grid), dim3(kGThreads), 0, ctx.stream, args)) != cudaSuccess) return e;
     }
   }
-  if (ga.num_tiles == 0) return cudaSuccess;
-  CUtensorMap map;
-  if ((e = make_x_tensor_map(&map, x, bf16, total_rows, ga.N)) != cudaSuccess) return e;
+  if (ga.num_tiles == 0 || map == nullptr) return cudaSuccess;
   const bool pdl = !skip_amax;
   if (bf16) {
-    if (mode == kCast1D) return launch_cast_t<uint16_t, kCast1D>(map, ga, pdl, ctx);
-    return launch_cast_t<uint16_t, kCast2D>(map, ga, pdl, ctx);
+    if (mode == kCast1D) return launch_cast_t<uint16_t, kCast1D>(*map, ga, pdl, ctx);
+    return launch_cast_t<uint16_t, kCast2D>(*map, ga, pdl, ctx);
   }
-  if (mode == kCast1D) return launch_cast_t<float, kCast1D>(map, ga, pdl, ctx);
-  return launch_cast_t<float, kCast2D>(map, ga, pdl, ctx);
+  if (mode == kCast1D) return launch_cast_t<float, kCast1D>(*map, ga, pdl, ctx);
+  return launch_cast_t<float, kCast2D>(*map, ga, pdl, ctx);
 }
 
 }  // namespace nvfp4

@@ -42,8 +42,10 @@ constexpr int64_t kGroupChunkVecs = 2048;
 // Zeroes the members' amax buffers and reduces max|x| per member into them
 // (skipped with skip_amax), then casts every member (mode kCast1D or
 // kCast2D): three launches whatever the number of members.  `ga` has every
-// field filled but tiles_n, num_tiles, num_chunks and the prefix sums.
-cudaError_t launch_grouped(const void* x, bool bf16, int mode, int64_t total_rows, GroupedArgs ga, bool skip_amax,
-                           const LaunchCtx& ctx);
+// field filled but tiles_n, num_tiles, num_chunks and the prefix sums;
+// `map` is the tensor map of x (all members' rows, make_x_tensor_map), or
+// null when x has no element.
+cudaError_t launch_grouped(const void* x, const CUtensorMap* map, bool bf16, int mode, GroupedArgs ga,
+                           bool skip_amax, const LaunchCtx& ctx);
 
 }  // namespace nvfp4

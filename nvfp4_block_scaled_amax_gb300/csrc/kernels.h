@@ -61,10 +61,19 @@ struct CastArgs {
   int tiles_n, num_tiles;
 };
 
-// Fused row-wise + column-wise cast of x (TMA tiles of 128 x 128 elements)
-// reading the per-tensor amax from args.amax_row / args.amax_col.  `pdl`:
-// launched as a programmatic dependent of the preceding amax kernel.
-cudaError_t launch_cast(const void* x, bool bf16, int mode, CastArgs args, bool pdl, const LaunchCtx& ctx);
+// Tensor map of x (M x N row-major, BF16 or FP32): dims {N, M}, box {128
+// bytes, 128 rows}, 128-byte swizzle, zero fill outside the tensor.  The
+// C-ABI layer encodes it before it enqueues anything for a call, so that a
+// call whose map cannot be encoded launches nothing.  Needs a 16-byte
+// aligned x and N * element size a multiple of 16 bytes (N % 16 == 0 is
+// validated first).
+cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N);
+
+// Fused row-wise + column-wise cast of x (TMA tiles of 128 x 128 elements,
+// `map` from make_x_tensor_map) reading the per-tensor amax from
+// args.amax_row / args.amax_col.  `pdl`: launched as a programmatic
+// dependent of the preceding amax kernel.
+cudaError_t launch_cast(const CUtensorMap& map, bool bf16, int mode, CastArgs args, bool pdl, const LaunchCtx& ctx);
 
 // Scratch of the single-pass kernels (a 64-byte header, zeroed before first
 // use, then kept consistent by the kernels themselves): the grid barrier's
@@ -84,12 +93,13 @@ static_assert(sizeof(SinglePassWorkspace) == kSinglePassHeaderBytes, "workspace 
 
 // One persistent launch: per-tensor amax of x (written to args.amax_row /
 // args.amax_col) and the fused cast (1D or 2D), x read from HBM once.
-cudaError_t launch_single_pass(const void* x, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
+cudaError_t launch_single_pass(const CUtensorMap& map, bool bf16, int mode, CastArgs args, SinglePassWorkspace* ws,
                                const LaunchCtx& ctx);
 // The same for the Hadamard quantize (BF16): max|x| into args.amax_row,
 // max|RHT(x)| into args.amax_col, then the row-wise cast of x and the
 // column-wise cast of the transformed columns.
-cudaError_t launch_single_pass_rht(const void* x, CastArgs args, SinglePassWorkspace* ws, const LaunchCtx& ctx);
+cudaError_t launch_single_pass_rht(const CUtensorMap& map, CastArgs args, SinglePassWorkspace* ws,
+                                   const LaunchCtx& ctx);
 // CTAs the single-pass kernel uses for an M x N input.
 int single_pass_grid(int64_t M, int64_t N, const LaunchCtx& ctx);
 

@@ -33,7 +33,9 @@ std::mutex g_scratch_mu;
 
 // Once per device, with that device current: the device address of the
 // array.  In host code the symbol itself is only a host-side stand-in, never
-// a device address.
+// a device address.  The address is that of the device's primary context at
+// the time of the first call; it is not looked up again, so a
+// cudaDeviceReset() of that device leaves it stale (documented in nvfp4.h).
 nvfp4_status scratch_for_current_device(void** ptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;

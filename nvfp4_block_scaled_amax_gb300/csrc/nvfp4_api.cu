@@ -75,8 +75,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Checks common to the quantize entry points.  `need_m16` / `need_n16`: the
-// operation blocks along that dimension.
+// Checks common to the quantize entry points.  N % 16 == 0 whatever the
+// directions: row-wise blocks span 16 columns, and every cast stages x by
+// TMA, whose row pitch must be a multiple of 16 bytes; column-wise blocks
+// span 16 rows (M % 16 == 0).  Row-wise alone takes any M.
 nvfp4_status check_quantize(const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,
                             unsigned flags, unsigned allowed_flags) {
   if (out == nullptr) return NVFP4_ERR_NULL;
@@ -84,11 +86,11 @@ nvfp4_status check_quantize(const void* x, int dtype, int64_t M, int64_t N, cons
   if (!(flags & (NVFP4_ROWWISE | NVFP4_COLWISE))) return NVFP4_ERR_FLAGS;
   if (dtype != NVFP4_BF16 && dtype != NVFP4_FP32) return NVFP4_ERR_DTYPE;
   if (M < 0 || N < 0 || M >= kMaxDim || N >= kMaxDim) return NVFP4_ERR_SHAPE;
+  if (N % 16 != 0) return NVFP4_ERR_SHAPE;
   if (M > 0 && N > 0 && x == nullptr) return NVFP4_ERR_NULL;
   if (x != nullptr && !aligned16(x)) return NVFP4_ERR_ALIGN;
   const bool row = flags & NVFP4_ROWWISE, col = flags & NVFP4_COLWISE;
   if (row) {
-    if (N % 16 != 0) return NVFP4_ERR_SHAPE;
     if (out->amax_row == nullptr) return NVFP4_ERR_NULL;
     if (M > 0 && N > 0 && (out->data_row == nullptr || out->scale_row == nullptr)) return NVFP4_ERR_NULL;
     if (!aligned16(out->data_row) || !aligned16(out->scale_row) || !aligned16(out->amax_row))
@@ -103,6 +105,42 @@ nvfp4_status check_quantize(const void* x, int dtype, int64_t M, int64_t N, cons
   }
   if (row && col && out->amax_row == out->amax_col) return NVFP4_ERR_FLAGS;
   if ((flags & NVFP4_SWIZZLED) && (M % 128 != 0 || N % 128 != 0)) return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
+// Tensor map of x for a call, encoded before the call enqueues anything (so a
+// map that cannot be encoded leaves every buffer untouched).  Encoding is a
+// driver call of about a microsecond and callers quantize the same buffers
+// over and over, so each thread keeps its last few maps, keyed by what the
+// map encodes (address, shape, element type): a map holds no device state.
+struct MapEntry {
+  CUtensorMap map;
+  const void* x;
+  int64_t M, N;
+  int bf16;
+  int used;
+};
+constexpr int kMapCache = 8;
+thread_local MapEntry t_maps[kMapCache];
+thread_local int t_map_next = 0;
+
+nvfp4_status x_map(const void* x, bool bf16, int64_t M, int64_t N, CUtensorMap* map) {
+  for (int i = 0; i < kMapCache; ++i) {
+    const MapEntry& e = t_maps[i];
+    if (e.used && e.x == x && e.M == M && e.N == N && e.bf16 == (int)bf16) {
+      *map = e.map;
+      return NVFP4_OK;
+    }
+  }
+  if (make_x_tensor_map(map, x, bf16, M, N) != cudaSuccess) return NVFP4_ERR_CUDA;
+  MapEntry& e = t_maps[t_map_next];
+  t_map_next = (t_map_next + 1) % kMapCache;
+  e.map = *map;
+  e.x = x;
+  e.M = M;
+  e.N = N;
+  e.bf16 = (int)bf16;
+  e.used = 1;
   return NVFP4_OK;
 }
 
@@ -125,6 +163,8 @@ nvfp4_status quantize_per_tensor(int mode, const void* x, int dtype, int64_t M, 
   float* a_row = row ? out->amax_row : nullptr;
   float* a_col = col ? out->amax_col : nullptr;
   const bool skip = flags & NVFP4_SKIP_AMAX;
+  CUtensorMap map;
+  if (M > 0 && N > 0 && (st = x_map(x, bf16, M, N, &map)) != NVFP4_OK) return st;
   if (!skip) {
     cudaError_t e;
     if (mode == kCastRHT && col && M > 0 && N > 0)
@@ -153,7 +193,7 @@ nvfp4_status quantize_per_tensor(int mode, const void* x, int dtype, int64_t M, 
   // output is the 1D cast of x (amax max|x|), by the kernel that has no
   // tensor-core column pass.
   const int cast_mode = (mode == kCastRHT && !col) ? kCast1D : mode;
-  return from_cuda(launch_cast(x, bf16, cast_mode, a, /*pdl=*/!skip, ctx));
+  return from_cuda(launch_cast(map, bf16, cast_mode, a, /*pdl=*/!skip, ctx));
 }
 
 nvfp4_status quantize_single_pass(int mode, const void* x, int dtype, int64_t M, int64_t N,
@@ -187,7 +227,9 @@ nvfp4_status quantize_single_pass(int mode, const void* x, int dtype, int64_t M,
   a.rowwise = row;
   a.colwise = col;
   a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
-  return from_cuda(launch_single_pass(x, dtype == NVFP4_BF16, mode, a,
+  CUtensorMap map;
+  if ((st = x_map(x, dtype == NVFP4_BF16, M, N, &map)) != NVFP4_OK) return st;
+  return from_cuda(launch_single_pass(map, dtype == NVFP4_BF16, mode, a,
                                       static_cast<SinglePassWorkspace*>(workspace), ctx));
 }
 
@@ -198,7 +240,6 @@ nvfp4_status quantize_sr(int mode, const void* x, int dtype, int64_t M, int64_t 
   const unsigned allowed = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SWIZZLED | NVFP4_SKIP_AMAX;
   nvfp4_status st = check_quantize(x, dtype, M, N, out, flags, allowed);
   if (st != NVFP4_OK) return st;
-  if (N % 16 != 0) return NVFP4_ERR_SHAPE;
   if (mode == kCast2D && M % 16 != 0) return NVFP4_ERR_SHAPE;
   if (M > 0 && N > 0 && rbits == nullptr) return NVFP4_ERR_NULL;
   if (!aligned16(rbits)) return NVFP4_ERR_ALIGN;
@@ -209,6 +250,8 @@ nvfp4_status quantize_sr(int mode, const void* x, int dtype, int64_t M, int64_t 
   float* a_row = row ? out->amax_row : nullptr;
   float* a_col = col ? out->amax_col : nullptr;
   const bool skip = flags & NVFP4_SKIP_AMAX;
+  CUtensorMap map;
+  if (M > 0 && N > 0 && (st = x_map(x, dtype == NVFP4_BF16, M, N, &map)) != NVFP4_OK) return st;
   if (!skip && launch_amax(x, dtype == NVFP4_BF16, M * N, a_row ? a_row : a_col, a_row ? a_col : nullptr, noop,
                            ctx) != cudaSuccess)
     return NVFP4_ERR_CUDA;
@@ -227,7 +270,7 @@ nvfp4_status quantize_sr(int mode, const void* x, int dtype, int64_t M, int64_t 
   a.rowwise = row;
   a.colwise = col;
   a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
-  return from_cuda(launch_cast_sr(x, dtype == NVFP4_BF16, mode, a, rbits, /*pdl=*/!skip, ctx));
+  return from_cuda(launch_cast_sr(map, dtype == NVFP4_BF16, mode, a, rbits, /*pdl=*/!skip, ctx));
 }
 
 static_assert(NVFP4_MAX_GROUPS == kMaxGroups, "member table size");
@@ -286,7 +329,11 @@ nvfp4_status quantize_grouped(int mode, const void* x, int dtype, int64_t N, int
   ga.rowwise = row;
   ga.colwise = col;
   ga.swizzled = (flags & NVFP4_SWIZZLED) != 0;
-  return from_cuda(launch_grouped(x, dtype == NVFP4_BF16, mode, total, ga, (flags & NVFP4_SKIP_AMAX) != 0, ctx));
+  CUtensorMap map;
+  const bool any = total > 0 && N > 0;
+  if (any && (st = x_map(x, dtype == NVFP4_BF16, total, N, &map)) != NVFP4_OK) return st;
+  return from_cuda(launch_grouped(x, any ? &map : nullptr, dtype == NVFP4_BF16, mode, ga,
+                                  (flags & NVFP4_SKIP_AMAX) != 0, ctx));
 }
 
 }  // namespace
@@ -442,7 +489,9 @@ nvfp4_status nvfp4_quantize_rht_single_pass(const void* x, int dtype, int64_t M,
   a.colwise = 1;
   a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
   a.sign_mask = sign_mask & 0xFFFFu;
-  return from_cuda(launch_single_pass_rht(x, a, static_cast<SinglePassWorkspace*>(workspace), ctx));
+  CUtensorMap map;
+  if ((st = x_map(x, true, M, N, &map)) != NVFP4_OK) return st;
+  return from_cuda(launch_single_pass_rht(map, a, static_cast<SinglePassWorkspace*>(workspace), ctx));
 }
 
 nvfp4_status nvfp4_quantize_row_scaled(const void* x, int dtype, int64_t M, int64_t N, const nvfp4_output* out,

@@ -359,13 +359,8 @@ cudaError_t launch_t(const CUtensorMap& map, const CastArgs& a, const uint8_t* r
 
 }  // namespace
 
-cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N);
-
-cudaError_t launch_cast_sr(const void* x, bool bf16, int mode, CastArgs args, const uint8_t* rbits, bool pdl,
-                           const LaunchCtx& ctx) {
-  CUtensorMap map;
-  cudaError_t e = make_x_tensor_map(&map, x, bf16, args.M, args.N);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_cast_sr(const CUtensorMap& map, bool bf16, int mode, CastArgs args, const uint8_t* rbits,
+                           bool pdl, const LaunchCtx& ctx) {
   const int64_t tiles_m = (args.M + kTile - 1) / kTile, tiles_n = (args.N + kTile - 1) / kTile;
   args.tiles_n = (int)tiles_n;
   args.num_tiles = (int)(tiles_m * tiles_n);

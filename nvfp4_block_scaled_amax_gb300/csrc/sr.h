@@ -11,7 +11,7 @@ namespace nvfp4 {
 // cast.  Reads the per-tensor amax from args.amax_row / args.amax_col; `pdl`:
 // launched as a programmatic dependent of the preceding amax kernel.
 // N % 16 == 0; rbits 16-byte aligned, M x N bytes.
-cudaError_t launch_cast_sr(const void* x, bool bf16, int mode, CastArgs args, const uint8_t* rbits, bool pdl,
-                           const LaunchCtx& ctx);
+cudaError_t launch_cast_sr(const CUtensorMap& map, bool bf16, int mode, CastArgs args, const uint8_t* rbits,
+                           bool pdl, const LaunchCtx& ctx);
 
 }  // namespace nvfp4

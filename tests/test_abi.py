@@ -130,6 +130,14 @@ def test_quantize_validation(lib):
     assert q1d(lib, M=-1) == ERR_SHAPE
     assert q1d(lib, N=24, flags=ROW) == ERR_SHAPE                # row blocks need N % 16
     assert q1d(lib, M=24, flags=COL) == ERR_SHAPE                # column blocks need M % 16
+    # N % 16 whatever the directions: x is staged through a tensor map (row
+    # pitch a multiple of 16 bytes) and the BF16 casts own 16 columns per lane
+    assert q1d(lib, N=24, flags=COL) == ERR_SHAPE
+    assert q1d(lib, dtype=1, N=20, flags=COL) == ERR_SHAPE
+    assert q1d(lib, N=8, flags=COL | SKIP) == ERR_SHAPE
+    assert lib.nvfp4_quantize_1d_single_pass(X, 0, 256, 24, ctypes.byref(out(lib)), COL, None, A, None) == ERR_SHAPE
+    assert lib.nvfp4_quantize_2d_single_pass_noalloc(X, 0, 256, 40, ctypes.byref(out(lib)), COL, None,
+                                                     None) == ERR_SHAPE
     assert q1d(lib, x=X + 8) == ERR_ALIGN
     assert q1d(lib, o=out(lib, data_col=D + 4)) == ERR_ALIGN
     assert q1d(lib, o=out(lib, scale_row=0)) == ERR_NULL
