@@ -10,7 +10,8 @@ import torch
 
 import nvfp4_block_scaled_amax_gb300 as nv
 from nvfp4_block_scaled_amax_gb300 import inputs
-from nvfp4_testutil import assert_quantize_equal, bits, compare_rht_codes, np_
+from nvfp4_testutil import assert_quantize_equal, bits, check_rht_columns, np_
+from nvfp4_testutil import scales_compact as _compact
 
 pytestmark = pytest.mark.gpu
 
@@ -28,6 +29,7 @@ def _x(M, N, dtype, seed, kind="randn"):
 
 def _flags():
     return [(True, True), (True, False), (False, True)]
+
 
 
 @pytest.mark.parametrize("M,N", SHAPES)
@@ -78,9 +80,9 @@ def test_rht_matches_oracle(oracle_mod, M, N, path):
         torch.cuda.synchronize()
         assert_quantize_equal(oracle_mod, q, ref, swizzled, rowwise=True, colwise=False, what="rht row")
         np.testing.assert_array_equal(np_(q.amax_col), ref["amax_col"])
-        sc_ref = oracle_mod.swizzle(ref["col_scale"]) if swizzled else ref["col_scale"].reshape(-1)
-        nd, ns = compare_rht_codes(np_(q.data_col), ref["col_data"], np_(q.scale_col), sc_ref)
-        assert nd <= max(1, 1e-4 * M * N) and ns <= nd
+        c = check_rht_columns(oracle_mod, bits(x), mask, np_(q.data_col),
+                              _compact(oracle_mod, np_(q.scale_col), N, M // 16, swizzled), ref)
+        assert c["codes_differing"] <= 1e-4 * M * N
 
 
 def test_rht_single_pass_reuse_and_reloads(oracle_mod):
@@ -103,9 +105,9 @@ def test_rht_single_pass_reuse_and_reloads(oracle_mod):
                 assert_quantize_equal(oracle_mod, q, ref, swizzled, rowwise=True, colwise=False,
                                       what=f"rht {M}x{N} call {calls}")
                 np.testing.assert_array_equal(np_(q.amax_col), ref["amax_col"])
-                sc_ref = oracle_mod.swizzle(ref["col_scale"]) if swizzled else ref["col_scale"].reshape(-1)
-                nd, ns = compare_rht_codes(np_(q.data_col), ref["col_data"], np_(q.scale_col), sc_ref)
-                assert nd <= max(1, 1e-4 * M * N) and ns <= nd
+                c = check_rht_columns(oracle_mod, bits(x), mask, np_(q.data_col),
+                                      _compact(oracle_mod, np_(q.scale_col), N, M // 16, swizzled), ref)
+                assert c["codes_differing"] <= 1e-4 * M * N
     w = ws.view(torch.int32).cpu()
     assert int(w[0]) == calls                       # one generation per call
     assert int(w[2 + (calls & 1)]) == 0             # the next call's arrival count is clear
@@ -314,3 +316,24 @@ def test_cuda_graph_replay_with_stable_pointers(oracle_mod):
 
 def test_device_status_clean():
     assert nv.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("path", ["two_pass", "single_pass"])
+def test_rejected_shape_writes_nothing(path):
+    """A column-wise-only call with N % 16 != 0 is rejected on the host
+    before anything is enqueued ("Write both NVFP4 amax buffers", Changes:
+    a call that must not write leaves both amax buffers untouched): the
+    status is NVFP4_ERR_SHAPE and no buffer changes."""
+    M, N = 64, 24
+    x = _x(M, N, torch.bfloat16, seed=1).cuda()
+    q = nv.empty(M, 32, rowwise=False, colwise=True, device="cuda")   # buffers large enough for N = 32
+    q.data_col.fill_(0x5A)
+    q.scale_col.fill_(0x5A)
+    q.amax_col.fill_(-7.0)
+    q.N = N
+    with pytest.raises(nv.NVFP4Error) as err:
+        nv.quantize(x, "1d", rowwise=False, colwise=True, out=q, path=path)
+    assert err.value.status == 2
+    torch.cuda.synchronize()
+    assert q.amax_col.item() == -7.0
+    assert bool((q.data_col == 0x5A).all()) and bool((q.scale_col == 0x5A).all())
