@@ -82,6 +82,9 @@ def lib() -> ctypes.CDLL:
             L.oracle_hadamard16.restype = ctypes.c_int
             L.oracle_rht16.argtypes = [f32p, ctypes.c_uint32, ctypes.c_int, f32p]
             L.oracle_rht16.restype = None
+            L.oracle_rht_columns.argtypes = [vp, ctypes.c_int, i64, i64, ctypes.c_uint32, ctypes.c_int, vp, i64,
+                                             f32p]
+            L.oracle_rht_columns.restype = ctypes.c_int
             L.oracle_quantize.argtypes = [
                 ctypes.c_int, vp, ctypes.c_int, i64, i64,
                 ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_uint32,
@@ -183,6 +186,23 @@ def rht16(v: np.ndarray, mask: int, round_bf16: bool) -> np.ndarray:
     t = np.empty(16, dtype=np.float32)
     lib().oracle_rht16(_ptr(v), mask & 0xFFFF, int(round_bf16), _ptr(t))
     return t
+
+
+def rht_columns(x: np.ndarray, mask: int, round_bf16: bool, cols: np.ndarray | None = None) -> np.ndarray:
+    """The column-block RHT of the columns ``cols`` of x (all when None), as
+    a [len(cols), M] float32 array (row k = column cols[k] of x transformed):
+    rounded to BF16 like the column-wise quantize reads them, or the FP32 sums
+    before that rounding (round_bf16=False)."""
+    x = np.ascontiguousarray(x)
+    M, N = x.shape
+    ids = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nc = N if ids is None else ids.size
+    out = np.empty((nc, M), dtype=np.float32)
+    rc = lib().oracle_rht_columns(_ptr(x), _dtype_code(x), M, N, mask & 0xFFFF, int(round_bf16), _ptr(ids),
+                                  0 if ids is None else ids.size, _ptr(out))
+    if rc != 0:
+        raise ValueError("RHT columns need M % 16 == 0")
+    return out
 
 
 def encode_array(v: np.ndarray, fmt: str) -> np.ndarray:

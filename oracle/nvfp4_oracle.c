@@ -330,6 +330,29 @@ static void load_rht_column(const void* x, int dtype, int64_t M, int64_t N,
   }
 }
 
+/* Exposed for the tests: the transformed columns col_ids[0..n-1] of x (all
+ * N columns when col_ids is NULL), out[k * M + y] = row y of column
+ * col_ids[k] after the column-block RHT -- the values the column-wise quantize
+ * reads (load_rht_column) when round_bf16 matches the input type, or, with
+ * round_bf16 = 0, the FP32 sums before that rounding.  The RHT tolerance
+ * ("Write both NVFP4 amax buffers", review reply: the post-RHT amax pair;
+ * codes may differ by one E2M1 step at rounding ties only) is stated in terms
+ * of those pre-rounding values.  Returns -1 when M % 16 != 0. */
+int oracle_rht_columns(const void* x, int dtype, int64_t M, int64_t N, uint32_t mask, int round_bf16,
+                       const int64_t* col_ids, int64_t n, float* out) {
+  if (M < 0 || N < 0 || M % 16 != 0) return -1;
+  int64_t nc = col_ids ? n : N;
+  float v[16];
+  for (int64_t k = 0; k < nc; ++k) {
+    int64_t j = col_ids ? col_ids[k] : k;
+    for (int64_t b = 0; b < M / 16; ++b) {
+      for (int i = 0; i < 16; ++i) v[i] = load_elem(x, dtype, (16 * b + i) * N + j);
+      rht_block(v, mask, round_bf16, out + k * M + 16 * b);
+    }
+  }
+  return 0;
+}
+
 /* max|RHT(x)| over all column blocks. */
 float oracle_rht_amax(const void* x, int dtype, int64_t M, int64_t N, uint32_t mask) {
   float* col = (float*)malloc(sizeof(float) * (size_t)(M > 0 ? M : 1));

@@ -74,6 +74,11 @@ MUTANTS = {
     # RHT: column amax taken before the transform
     "rht_amax_untransformed": ("amax_col = (mode == MODE_RHT) ? oracle_rht_amax(x, dtype, M, N, sign_mask) : amax_row;",
                                "amax_col = amax_row;"),
+    # RHT columns exposed for the tolerance check: a block read one row off
+    "rht_columns_row_offset": ("for (int i = 0; i < 16; ++i) v[i] = load_elem(x, dtype, (16 * b + i) * N + j);\n"
+                               "      rht_block(v, mask, round_bf16",
+                               "for (int i = 0; i < 16; ++i) v[i] = load_elem(x, dtype, (16 * b + (i + 1) % 16) * N + j);\n"
+                               "      rht_block(v, mask, round_bf16"),
     # swizzle: the two row terms of the 128x4 tile swapped
     "swizzle_row_terms": ("(r % 32) * 16 + ((r % 128) / 32) * 4", "(r % 32) * 4 + ((r % 128) / 32) * 16"),
     # stochastic rounding: a byte equal to 256 f also rounds up

@@ -191,6 +191,50 @@ def test_rht_matches_restatement(oracle_mod, M, N, mask):
     np.testing.assert_array_equal(out["col_scale"], sT)
 
 
+@pytest.mark.parametrize("M,N,mask", [(16, 16, 0), (32, 48, 0xBEEF), (64, 64, 0x1234)])
+def test_rht_columns_match_restatement_when_exact(oracle_mod, M, N, mask):
+    # small integers times 2^-3: every Hadamard sum is exact in FP32, so the
+    # values before and after the BF16 rounding are the FP64 product's
+    rng = np.random.default_rng(M + N + mask)
+    Xf = (rng.integers(-40, 41, (M, N)) / 8.0).astype(np.float32)
+    x = bf16_bits(torch.from_numpy(Xf).to(torch.bfloat16))
+    X = to_f32(x)
+    np.testing.assert_array_equal(oracle_mod.rht_columns(x, mask, False), np_rht_columns(X, mask, False))
+    np.testing.assert_array_equal(oracle_mod.rht_columns(x, mask, True), np_rht_columns(X, mask, True))
+    cols = np.array([N - 1, 0, N // 2])
+    np.testing.assert_array_equal(oracle_mod.rht_columns(x, mask, True, cols),
+                                  np_rht_columns(X, mask, True)[cols])
+
+
+@pytest.mark.parametrize("M,N,mask", [(64, 48, 0x5A5A), (256, 32, 0xFFFF)])
+def test_rht_columns_on_random_data(oracle_mod, M, N, mask):
+    """BF16 values whose exponents spread over 2^-20..2^11, so that many FP32
+    Hadamard sums round: they stay within the bound of a 16-term FP32
+    summation (15 u sum|terms|, u = 2^-24) of the exact transform; the
+    rounded values are the BF16 rounding (PyTorch's cast) of the FP32 sums;
+    their maximum is the column amax, and the column-wise output is the 1D
+    quantization of the rounded columns."""
+    rng = np.random.default_rng(M * N)
+    Xf = (rng.standard_normal((M, N)) * 2.0 ** rng.integers(-20, 12, (M, N))).astype(np.float32)
+    x = bf16_bits(torch.from_numpy(Xf).to(torch.bfloat16))
+    X = to_f32(x)
+    t32 = oracle_mod.rht_columns(x, mask, False)
+    t16 = oracle_mod.rht_columns(x, mask, True)
+    from oracle import hadamard16
+    sign = np.array([-1.0 if (mask >> i) & 1 else 1.0 for i in range(16)])
+    u = X.astype(np.float64).reshape(M // 16, 16, N) * sign[None, :, None]
+    exact = (np.einsum("oi,kin->kon", hadamard16().astype(np.float64), u) / 4.0).reshape(M, N).T
+    bound = 15 * 2.0 ** -24 * np.repeat(np.abs(u).sum(axis=1) / 4.0, 16, axis=0).T
+    assert np.all(np.abs(t32.astype(np.float64) - exact) <= bound)
+    assert np.any(t32.astype(np.float64) != exact)           # the case is not trivially exact
+    np.testing.assert_array_equal(t16, torch.from_numpy(t32).to(torch.bfloat16).float().numpy())
+    assert np.abs(t16).max() == oracle_mod.rht_amax(x, mask)
+    out = oracle_mod.quantize("rht", x, sign_mask=mask)
+    dT, sT = np_quantize_1d_rows(t16, np.full(N, np_global(np.abs(t16).max()), np.float32))
+    np.testing.assert_array_equal(out["col_data"], dT)
+    np.testing.assert_array_equal(out["col_scale"], sT)
+
+
 # ---------------------------------------------------------------------------
 # closed forms and invariants
 # ---------------------------------------------------------------------------
