@@ -210,6 +210,65 @@ def host_us_per_call(step, n=200):
     return round(1e6 * t / n, 2)
 
 
+def host_costs(nv, spec, x, q, mask, step, stream):
+    """Host microseconds per call, three ways: the Python ``quantize``; a
+    ``QuantizePlan`` bound once to the tensors; the C entry point itself,
+    called through ctypes with its arguments built once (argument checks,
+    tensor-map lookup and the kernel launch)."""
+    import ctypes
+
+    from nvfp4_block_scaled_amax_gb300 import _lib
+    mode = spec["mode"]
+    colwise = mode != "row_scaled"
+    plan = nv.QuantizePlan(x, mode, rowwise=True, colwise=colwise, swizzled=spec["swizzled"], sign_mask=mask,
+                           out=q)
+    sp = stream.cuda_stream
+    plan_us = host_us_per_call(lambda: plan(sp))
+    L = _lib.load()
+    fn, args = plan._fn, plan._args + (ctypes.c_void_p(sp),)
+    c_us = host_us_per_call(lambda: fn(*args))
+    return {"python_quantize": host_us_per_call(step), "python_plan": plan_us, "c_abi_via_ctypes": c_us}
+
+
+def steady_state(nv, spec, x_host, dev, stream, steps):
+    """The same quantize called back to back with no L2 flush, rotating over
+    three input and three output sets (3 x (input + outputs) > the 129 MB
+    L2), so each call's reads come from HBM and the previous calls' dirty
+    outputs are written back while it runs: ms per call from two events
+    around all the calls."""
+    import torch
+    mode = spec["mode"]
+    colwise = mode != "row_scaled"
+    mask = 0
+    if mode == "rht":
+        from nvfp4_block_scaled_amax_gb300 import inputs
+        mask = inputs.sign_mask_from_seed(spec["seed"])
+    xs = [x_host.to(dev) for _ in range(3)]
+    qs = [nv.empty(spec["M"], spec["N"], colwise=colwise, row_scaled=mode == "row_scaled",
+                   swizzled=spec["swizzled"], device=dev) for _ in range(3)]
+    calls = [(lambda xi=xi, qi=qi: nv.quantize(xi, mode, colwise=colwise, swizzled=spec["swizzled"],
+                                               sign_mask=mask, out=qi)) for xi, qi in zip(xs, qs)]
+    n = max(30, 3 * steps)
+    for k in range(9):
+        calls[k % 3]()
+    torch.cuda.synchronize()
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(2_000_000)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for k in range(n):
+        calls[k % 3]()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    gbs = workload_bytes(spec) / (ms / 1e3) / 1e9
+    peak, _ = measured_peaks()
+    del xs, qs
+    torch.cuda.empty_cache()
+    return {"ms_per_call": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), "calls": n,
+            "how": "back to back, no flush; 3 input and output sets rotated (more than L2 in all)"}
+
+
 def bench_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -281,7 +340,8 @@ def bench_ours(args, rank, world, local_rank):
 
     # e2e: host buffers through the public API, copies inside the timed region
     e2e = None if args.no_e2e else bench_e2e(nv, spec, x_host, q, mask, args, dev, flush)
-    host_us = host_us_per_call(step)
+    host_us = host_costs(nv, spec, x, q, mask, step, stream)
+    steady = steady_state(nv, spec, x_host, dev, stream, args.steps)
 
     peak, peak_kind = measured_peaks()
     ms_per_step = total_ms / args.steps
@@ -310,7 +370,9 @@ def bench_ours(args, rank, world, local_rank):
                      "traffic": ncu_traffic(args.workload), "two_pass_ms": split},
         "e2e": e2e,
         "gpu_launches": gpu_launches,
-        "host_us_per_call": host_us,
+        "host_us_per_call": host_us["c_abi_via_ctypes"],
+        "host_us": host_us,
+        "steady_state": steady,
         "wall_s_timed": round(wall, 3),
     }
     if rank == 0:
@@ -446,6 +508,28 @@ def time_oracle(spec, x_host, rows):
     return time.perf_counter() - t0
 
 
+def host_cpu():
+    """The host's logical core count and CPU model name (lscpu, else
+    /proc/cpuinfo, else the platform string)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    return {"host_cores": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine()}
+
+
 def cpu_baseline(spec, x_host, budget_s):
     import oracle
     oracle.build()
@@ -457,7 +541,8 @@ def cpu_baseline(spec, x_host, budget_s):
     frac = target / M
     gbs = workload_bytes(spec) * frac / t / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {target} of {M} rows ({N} columns), {t:.1f} s, single-threaded C oracle"}
+            "sample": f"first {target} of {M} rows ({N} columns), {t:.1f} s, single-threaded C oracle",
+            **host_cpu()}
 
 
 def bench_reference(args, rank):
@@ -486,7 +571,7 @@ def bench_reference(args, rank):
                        "swizzled": spec["swizzled"]},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **host_cpu()},
             "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -39,7 +39,7 @@ ROW_SCALED = 16
 BF16 = 0
 FP32 = 1
 
-__all__ = ["NVFP4Tensor", "NVFP4Error", "empty", "compute_amax", "compute_amax_rht", "quantize",
+__all__ = ["NVFP4Tensor", "NVFP4Error", "empty", "compute_amax", "compute_amax_rht", "quantize", "QuantizePlan",
            "single_pass_workspace", "reset_workspaces",
            "quantize_1d", "quantize_2d", "quantize_rht", "quantize_row_scaled", "quantize_grouped", "quantize_sr",
            "dequantize",
@@ -235,6 +235,86 @@ def quantize(x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: b
             raise ValueError(f"unknown mode {mode!r}")
     _lib.check(rc, f"nvfp4 quantize ({mode})")
     return out
+
+
+class QuantizePlan:
+    """A quantize call bound once to its tensors, for loops that repeat it.
+
+    ``quantize`` checks and marshals its arguments on every call (about
+    10 µs of Python); a plan does that once -- the C function, the pointers,
+    the flags, the output struct and, for the single-pass path, the
+    workspace -- and each call then only passes them to the library with the
+    stream.  The tensors must stay allocated, at the same addresses, for the
+    plan's lifetime (the plan keeps references to them).  Arguments as
+    ``quantize``; ``out`` defaults to buffers allocated here.
+
+        plan = QuantizePlan(x, "2d", swizzled=True)
+        plan()            # on x's device's current stream
+        plan(stream=s)    # a torch.cuda.Stream or a raw cudaStream_t handle
+    """
+
+    def __init__(self, x: torch.Tensor, mode: str = "1d", rowwise: bool = True, colwise: bool = True,
+                 swizzled: bool = False, sign_mask: int = 0, out: NVFP4Tensor | None = None,
+                 skip_amax: bool = False, noop: torch.Tensor | None = None, path: str = "auto",
+                 workspace: torch.Tensor | None = None):
+        if x.dim() != 2:
+            raise ValueError("x must be 2-D (M x N)")
+        M, N = x.shape
+        if mode == "row_scaled":
+            colwise = False
+        if out is None:
+            out = empty(M, N, rowwise, colwise, row_scaled=mode == "row_scaled", swizzled=swizzled,
+                        device=x.device)
+        out.swizzled = swizzled
+        _require_cuda(x, out.data_row, out.scale_row, out.amax_row, out.data_col, out.scale_col, out.amax_col,
+                      noop)
+        if path not in ("auto", "single_pass", "two_pass"):
+            raise ValueError(f"unknown path {path!r}")
+        flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLED if swizzled else 0) | \
+            (SKIP_AMAX if skip_amax else 0)
+        single = (mode in ("1d", "2d") or (mode == "rht" and path == "single_pass")) and not skip_amax and \
+            path != "two_pass"
+        if path == "single_pass" and not single:
+            raise ValueError("the single-pass path covers 1d / 2d / rht quantize without skip_amax")
+        L = _lib.load()
+        self.x, self.out, self.noop, self.device = x, out, noop, x.device
+        self._st = out.c_struct()
+        head = (_ptr(x), _dtype_code(x), M, N, ctypes.byref(self._st), flags)
+        if single:
+            dev = x.device if x.device.index is not None else torch.device("cuda", torch.cuda.current_device())
+            self.ws = workspace if workspace is not None else \
+                single_pass_workspace(dev, torch.cuda.current_stream(dev).cuda_stream)
+            _require_cuda(self.ws)
+            if mode == "rht":
+                self._fn, self._args = L.nvfp4_quantize_rht_single_pass, head + (sign_mask & 0xFFFF, _ptr(noop),
+                                                                                   _ptr(self.ws))
+            else:
+                fn = L.nvfp4_quantize_1d_single_pass if mode == "1d" else L.nvfp4_quantize_2d_single_pass
+                self._fn, self._args = fn, head + (_ptr(noop), _ptr(self.ws))
+        elif mode in ("1d", "2d", "row_scaled"):
+            fn = {"1d": L.nvfp4_quantize_1d, "2d": L.nvfp4_quantize_2d,
+                  "row_scaled": L.nvfp4_quantize_row_scaled}[mode]
+            self._fn, self._args = fn, head + (_ptr(noop),)
+        elif mode == "rht":
+            self._fn, self._args = L.nvfp4_quantize_rht, head + (sign_mask & 0xFFFF, _ptr(noop))
+        else:
+            raise ValueError(f"unknown mode {mode!r}")
+        self.mode = mode
+        self._dev_index = x.device.index if x.device.index is not None else torch.cuda.current_device()
+
+    def __call__(self, stream=None) -> NVFP4Tensor:
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device).cuda_stream
+        elif isinstance(stream, torch.cuda.Stream):
+            stream = stream.cuda_stream
+        if torch.cuda.current_device() != self._dev_index:
+            with _OnDevice(self.device):
+                rc = self._fn(*self._args, ctypes.c_void_p(stream))
+        else:
+            rc = self._fn(*self._args, ctypes.c_void_p(stream))
+        if rc != 0:
+            _lib.check(rc, f"nvfp4 quantize plan ({self.mode})")
+        return self.out
 
 
 def quantize_sr(x: torch.Tensor, rbits: torch.Tensor, mode: str = "1d", rowwise: bool = True,

@@ -88,19 +88,21 @@ struct FSmem {
   uint16_t* pre;     // [kPreTiles][64] 2D (BF16): 16x16 tile maxima found in phase A
 };
 
-// The two stage hooks the cast passes call (see wide_pass).
-template <class D, class W>
+// The stage hooks the cast passes call (see wide_pass).
+template <class D, class W, class St>
 struct StageHooksT {
   D done_fn;
   W wait_fn;
+  St staged_fn;
   const uint16_t* pre;  // 2D: the tile's 16x16 maxima found in phase A, or null
   __device__ __forceinline__ void data_done(uint32_t token) const { done_fn(token); }
   __device__ __forceinline__ void scale_wait() const { wait_fn(); }
+  __device__ __forceinline__ void scales_staged() const { staged_fn(); }
   __device__ __forceinline__ const uint16_t* tile_max() const { return pre; }
 };
-template <class D, class W>
-__device__ __forceinline__ StageHooksT<D, W> make_hooks(D d, W w, const uint16_t* pre = nullptr) {
-  return StageHooksT<D, W>{d, w, pre};
+template <class D, class W, class St>
+__device__ __forceinline__ StageHooksT<D, W, St> make_hooks(D d, W w, St st, const uint16_t* pre = nullptr) {
+  return StageHooksT<D, W, St>{d, w, st, pre};
 }
 
 
@@ -310,9 +312,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     auto scale_wait = [&] {
       scales_ok = sp::warp_wait_count(wbq, (unsigned)(WPT * (it >> 1)), a.status) && scales_ok;
     };
+    // 128x4 layout: once all of the group's warps have staged their scales,
+    // the last of them writes the tile's scales with one bulk copy per
+    // direction; the buffer is freed once the copies have read it (at that
+    // warp's next iteration)
+    auto staged = [&] {
+      if constexpr (kBulk)
+        sp::bulk_staged<WPT>(&sm.staged[grp * 2 + (it & 1)], grp * 2 + (it & 1), sc, a, r0, c0, do_row, do_col,
+                             pending_q);
+    };
     if constexpr (sizeof(T) == 2) {
       const auto hooks = make_hooks([&](uint32_t token) { ring.release(s, k - S, stream, token); }, scale_wait,
-                                    use_pre ? sm.pre + k * 64 : nullptr);
+                                    staged, use_pre ? sm.pre + k * 64 : nullptr);
       wide_pass_any<MODE, kBulk>(st, sm.rtab_row, smem_u32(sc), smem_u32(sc + kScRegion), a, r0, c0, g, do_row,
                                  do_col, cw, hooks);
     } else {
@@ -327,13 +338,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       *sm.abort_flag = 1;
       break;
     }
-    if constexpr (kBulk) {
-      // The group's last warp to finish staging writes the tile's scales
-      // with one bulk copy per direction; the buffer is freed once the
-      // copies have read it (at that warp's next iteration).
-      sp::bulk_staged<WPT>(&sm.staged[grp * 2 + (it & 1)], grp * 2 + (it & 1), sc, a, r0, c0, do_row, do_col,
-                           pending_q);
-    } else {
+    if constexpr (!kBulk) {
       sp::count_staged(&sm.staged[grp * 2 + (it & 1)]);
       if (k_prev >= 0 && !write_back(k_prev, it - 1)) {
         *sm.abort_flag = 1;

@@ -111,6 +111,8 @@ struct RowHooks {  // the row-wise wide pass: the stage is released after the co
   unsigned* status;
   __device__ __forceinline__ void data_done(uint32_t token) const { *tok ^= token; }
   __device__ __forceinline__ void scale_wait() const;
+  // the tile's scales (both directions) leave after the column pass
+  __device__ __forceinline__ void scales_staged() const {}
 };
 __device__ __forceinline__ void RowHooks::scale_wait() const { *ok = sp::warp_wait_count(wbq, want, status) && *ok; }
 

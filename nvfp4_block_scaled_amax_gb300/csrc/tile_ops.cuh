@@ -454,16 +454,22 @@ struct SubW {
   uint32_t a[8][4], b[8][4];  // [row k][BF16 pair]: halves A and B
 };
 
-__device__ __forceinline__ void load_sub_w(uint32_t stage, int wc, int trow, int j, int par, SubW& s) {
+// Returns a token computed from one word of every load: each 16-byte load
+// writes its four registers when it completes, so anything that depends on
+// the token comes after all sixteen loads have read shared memory.
+__device__ __forceinline__ uint32_t load_sub_w(uint32_t stage, int wc, int trow, int j, int par, SubW& s) {
   const uint32_t base = stage + wc * kBoxBytes + trow * 128;
   const uint32_t ca = (uint32_t)(2 * j + par) << 4, cb = ca ^ 16u;
+  uint32_t tok = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint4 va = lds128(base + 128 * k + (ca ^ (k << 4)));
     const uint4 vb = lds128(base + 128 * k + (cb ^ (k << 4)));
     s.a[k][0] = va.x; s.a[k][1] = va.y; s.a[k][2] = va.z; s.a[k][3] = va.w;
     s.b[k][0] = vb.x; s.b[k][1] = vb.y; s.b[k][2] = vb.z; s.b[k][3] = vb.w;
+    tok ^= va.x ^ vb.x;
   }
+  return tok;
 }
 
 // Codes of row k of one half (8 values), v0 in the low nibble.
@@ -497,6 +503,7 @@ __device__ __forceinline__ uint32_t col_pair_acc_w(const uint32_t (&w)[8][4], in
 struct NoHooks {
   __device__ __forceinline__ void data_done(uint32_t) const {}
   __device__ __forceinline__ void scale_wait() const {}
+  __device__ __forceinline__ void scales_staged() const {}
   __device__ __forceinline__ const uint16_t* tile_max() const { return nullptr; }
 };
 
@@ -539,7 +546,10 @@ __device__ __forceinline__ uint32_t stage_swz_offset(int r, int h) {
 // found while the tile was first read; else they are computed here.
 // kSwz (tiles inside x, 128x4 layout): the scales are staged as the tile's
 // two 512-byte atoms per direction, byte for byte as they are stored (see
-// stage_swz_offset), so that one bulk copy per direction writes them.
+// stage_swz_offset), so that one bulk copy per direction writes them; in 2D
+// the warp calls hooks.scales_staged() once its share is staged, before it
+// computes and stores any code (the bulk copy then runs meanwhile, and its
+// proxy fence waits on the staging stores only).
 template <int MODE, int kDirs, bool kInterior, bool kSwz = false, class Hooks = NoHooks>
 __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uint32_t sc_row, uint32_t sc_col,
                                           const CastArgs& a, int64_t r0, int64_t c0, float g, int warp,
@@ -549,7 +559,7 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
   const int wr = warp >> 1, wc = warp & 1, i = lane >> 2, j = lane & 3, par = i & 1;
   const int trow = 64 * wr + 8 * i, tcol = 64 * wc + 16 * j;
   SubW s;
-  load_sub_w(stage, wc, trow, j, par, s);
+  const uint32_t ltok = load_sub_w(stage, wc, trow, j, par, s);
 
   const int64_t M = a.M, N = a.N, y0 = r0 + trow, x0 = c0 + tcol;
   const int64_t srow = N / 2, scol = M / 2;
@@ -580,6 +590,7 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
     float m;
     if (pre != nullptr) {
       m = __uint_as_float((uint32_t)pre[(trow >> 4) * 8 + (tcol >> 4)] << 16);
+      hooks.data_done(ltok);  // the loads are complete: the stage may be refilled
     } else {
       uint32_t acc;
       m = wide_tile_max(s.a, s.b, acc);
@@ -589,26 +600,7 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
     // codes are the row-wise ones transposed)
     const uint32_t sb = block_scale(m, g);
     const float rf = rtab[sb];
-    uint32_t ca[8], cb[8], tok = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t wa = encode_half_row(s.a[k], rf);
-      const uint32_t wb = encode_half_row(s.b[k], rf);
-      if (kRow) put_row(k, wa, wb);
-      ca[k] = wa;
-      cb[k] = wb;
-      if (pre != nullptr) tok ^= wa ^ wb;
-    }
-    if (pre != nullptr) hooks.data_done(tok);  // each row's codes depend on its words
-    if (kCol) {
-      transpose_nibbles8x8(ca);
-      transpose_nibbles8x8(cb);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        put_col(c, par ? cb[c] : ca[c]);
-        put_col(8 + c, par ? ca[c] : cb[c]);
-      }
-    }
+    // the scales first, so that their write-back overlaps the codes
     if constexpr (kSwz) {
       // the four column blocks of a row (lanes j) and the four row blocks of
       // a column (lanes i >> 1) gathered into the 4-byte word they share
@@ -623,11 +615,30 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
         if (kRow) sts_u32(sc_row + stage_swz_offset(trow + 2 * j + t, tcol >> 6), wrow);
         if (kCol) sts_u32(sc_col + stage_swz_offset(tcol + 2 * i + t, trow >> 6), wcol);
       }
+      hooks.scales_staged();
     } else {
       hooks.scale_wait();
       if (par == 0) {
         if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sb);
         if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sb);
+      }
+    }
+    uint32_t ca[8], cb[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t wa = encode_half_row(s.a[k], rf);
+      const uint32_t wb = encode_half_row(s.b[k], rf);
+      if (kRow) put_row(k, wa, wb);
+      ca[k] = wa;
+      cb[k] = wb;
+    }
+    if (kCol) {
+      transpose_nibbles8x8(ca);
+      transpose_nibbles8x8(cb);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        put_col(c, par ? cb[c] : ca[c]);
+        put_col(8 + c, par ? ca[c] : cb[c]);
       }
     }
   } else {
@@ -707,6 +718,7 @@ __device__ __forceinline__ void wide_pass(uint32_t stage, const float* rtab, uin
         sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
       }
     }
+    if constexpr (kSwz) hooks.scales_staged();
   }
 }
 

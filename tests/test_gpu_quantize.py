@@ -337,3 +337,32 @@ def test_rejected_shape_writes_nothing(path):
     torch.cuda.synchronize()
     assert q.amax_col.item() == -7.0
     assert bool((q.data_col == 0x5A).all()) and bool((q.scale_col == 0x5A).all())
+
+
+@pytest.mark.parametrize("mode,path", [("1d", "auto"), ("2d", "auto"), ("rht", "auto"), ("row_scaled", "auto"),
+                                       ("2d", "two_pass"), ("rht", "single_pass")])
+def test_quantize_plan_matches_quantize(oracle_mod, mode, path):
+    """A QuantizePlan, bound once, gives what quantize gives, call after call
+    on the same (updated in place) input; on another stream too."""
+    M, N = 256, 384
+    x = _x(M, N, torch.bfloat16, seed=21, kind="outliers").cuda()
+    mask = 0x1357 if mode == "rht" else 0
+    plan = nv.QuantizePlan(x, mode, swizzled=True, sign_mask=mask, path=path)
+    s = torch.cuda.Stream()
+    for i, scale in enumerate((1.0, 0.5, 4.0)):
+        x.mul_(scale)                                   # powers of two: exact in BF16
+        if i == 2:
+            s.wait_stream(torch.cuda.current_stream())
+            q = plan(stream=s)
+            torch.cuda.current_stream().wait_stream(s)
+        else:
+            q = plan()
+        ref = nv.quantize(x, mode, swizzled=True, sign_mask=mask)
+        torch.cuda.synchronize()
+        for a, b in ((q.data_row, ref.data_row), (q.scale_row, ref.scale_row), (q.amax_row, ref.amax_row),
+                     (q.data_col, ref.data_col), (q.scale_col, ref.scale_col), (q.amax_col, ref.amax_col)):
+            if b is not None:
+                assert torch.equal(a, b)
+        assert_quantize_equal(oracle_mod, q, oracle_mod.quantize(mode, bits(x), colwise=mode != "row_scaled",
+                                                                 sign_mask=mask), True,
+                              colwise=mode not in ("row_scaled", "rht"))
