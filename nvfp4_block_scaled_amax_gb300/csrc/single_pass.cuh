@@ -105,14 +105,19 @@ struct StageRing {
     for (int bb = 0; bb < TileCfg<T>::kBoxes; ++bb)
       tma_load_2d(dst + bb * kBoxBytes, tmap, (int32_t)c0 + bb * TileCfg<T>::kBoxCols, (int32_t)r0, &full[s], pol);
   }
-  // Warp: done with stage s's tile.  The group's last warp loads tile `next`
-  // (if any) into the stage.  The count's address depends on `token`, a
-  // value computed from every word the warp read, so the count cannot be
-  // performed before those reads have completed.
+  // Warp (all lanes): done with stage s's tile.  The group's last warp
+  // loads tile `next` (if any) into the stage.  `token` is a value each lane
+  // computed from every word it read.  Lane 0 counts the warp out, but the
+  // lanes need not have run in step up to here (a lane-0-only branch
+  // earlier on can leave lane 0 ahead of the others), so the lanes' tokens
+  // are first combined by a warp-wide reduction, which waits for every lane
+  // and for its reads, and the count's address depends on the result.
   __device__ __forceinline__ void release(int s, int next, uint64_t pol, uint32_t token) const {
+    const uint32_t all = __reduce_or_sync(0xFFFFFFFFu, token);
+    __syncwarp();
     if ((threadIdx.x & 31) == 0) {
       uint32_t zero;
-      asm volatile("and.b32 %0, %1, 0;" : "=r"(zero) : "r"(token));
+      asm volatile("and.b32 %0, %1, 0;" : "=r"(zero) : "r"(all));
       if (atomicAdd(&loaded[s] + zero, 1u) == (unsigned)(WPT - 1)) {
         loaded[s] = 0;
         __threadfence_block();
