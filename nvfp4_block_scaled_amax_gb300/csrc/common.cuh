@@ -92,6 +92,35 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
   return out;
 }
 
+// Stochastic rounding to E2M1 with one random byte b (0..255) per value:
+// between neighbouring magnitudes lo <= |p| < hi the magnitude becomes hi
+// iff b < 256 f, f = (|p| - lo) / (hi - lo); |p| >= 6 gives 6; the sign of p
+// is kept.
+//
+// Carry form.  From 1 up, the E2M1 magnitudes are the FP32 values with a
+// single mantissa bit, so with u the bits of w = min(|p|, 6) the lower
+// neighbour is u's bits 22 and up and f is bits 21..0 over 2^22.  Adding
+// sr_offset(b) = ((255 - b) << 14) | (2^14 - 1) to u carries into bit 22
+// exactly when bits 21..0 exceed b << 14, that is when b < 256 f, and
+// (u + offset) >> 22 is then the code plus 252.  Below 1 the magnitudes
+// 0, 0.5, 1 are evenly spaced: v = w / 2 + 1/2 rounded up has the bits
+// 0x3F000000 + ceil(2^23 w), i.e. the code plus 252 in bits 22 and up and
+// ceil(2^22 f) below, which carries the same way (ceil(y) > n exactly when
+// y > n for an integer n).  max(v, w) is v below 1 and w from 1 up.  Every
+// step is exact; sr_code252 returns the code plus 252 (252..259).
+__device__ __forceinline__ uint32_t sr_offset(uint32_t b) { return ((b ^ 0xFFu) << 14) | 0x3FFFu; }
+// sr_offset of byte c (0..3) of a word, given the word's complement nw.
+__device__ __forceinline__ uint32_t sr_offset_nw(uint32_t nw, int c) {
+  return (((nw >> (8 * c)) & 0xFFu) << 14) | 0x3FFFu;
+}
+__device__ __forceinline__ uint32_t sr_code252(float abs_p, uint32_t offset) {
+  const float w = fminf(abs_p, 6.0f);
+  return (__float_as_uint(fmaxf(__fmaf_ru(w, 0.5f, 0.5f), w)) + offset) >> 22;
+}
+__device__ __forceinline__ uint32_t e2m1_sr(float p, uint32_t offset) {
+  return (sr_code252(fabsf(p), offset) - 252u) | ((__float_as_uint(p) >> 28) & 8u);
+}
+
 // ---------------------------------------------------------------------------
 // BF16 helpers (a 32-bit word holds two BF16 values, the lower address in
 // the low half)

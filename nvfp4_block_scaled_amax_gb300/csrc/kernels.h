@@ -68,6 +68,10 @@ struct CastArgs {
 // aligned x and N * element size a multiple of 16 bytes (N % 16 == 0 is
 // validated first).
 cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_t M, int64_t N);
+// Tensor map of an M x N byte matrix (row pitch N): box 128 x 128 bytes,
+// 128-byte swizzle, zero fill outside.  Needs a 16-byte aligned base and
+// N % 16 == 0.
+cudaError_t make_byte_tensor_map(CUtensorMap* map, const void* p, int64_t M, int64_t N);
 
 // Fused row-wise + column-wise cast of x (TMA tiles of 128 x 128 elements,
 // `map` from make_x_tensor_map) reading the per-tensor amax from

@@ -117,31 +117,36 @@ struct MapEntry {
   CUtensorMap map;
   const void* x;
   int64_t M, N;
-  int bf16;
+  int kind;  // element type: 0 FP32, 1 BF16, 2 byte
   int used;
 };
 constexpr int kMapCache = 8;
 thread_local MapEntry t_maps[kMapCache];
 thread_local int t_map_next = 0;
 
-nvfp4_status x_map(const void* x, bool bf16, int64_t M, int64_t N, CUtensorMap* map) {
+nvfp4_status cached_map(const void* x, int kind, int64_t M, int64_t N, CUtensorMap* map) {
   for (int i = 0; i < kMapCache; ++i) {
     const MapEntry& e = t_maps[i];
-    if (e.used && e.x == x && e.M == M && e.N == N && e.bf16 == (int)bf16) {
+    if (e.used && e.x == x && e.M == M && e.N == N && e.kind == kind) {
       *map = e.map;
       return NVFP4_OK;
     }
   }
-  if (make_x_tensor_map(map, x, bf16, M, N) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const cudaError_t r =
+      kind == 2 ? make_byte_tensor_map(map, x, M, N) : make_x_tensor_map(map, x, kind == 1, M, N);
+  if (r != cudaSuccess) return NVFP4_ERR_CUDA;
   MapEntry& e = t_maps[t_map_next];
   t_map_next = (t_map_next + 1) % kMapCache;
   e.map = *map;
   e.x = x;
   e.M = M;
   e.N = N;
-  e.bf16 = (int)bf16;
+  e.kind = kind;
   e.used = 1;
   return NVFP4_OK;
+}
+nvfp4_status x_map(const void* x, bool bf16, int64_t M, int64_t N, CUtensorMap* map) {
+  return cached_map(x, bf16 ? 1 : 0, M, N, map);
 }
 
 nvfp4_status quantize_per_tensor(int mode, const void* x, int dtype, int64_t M, int64_t N,
@@ -250,8 +255,9 @@ nvfp4_status quantize_sr(int mode, const void* x, int dtype, int64_t M, int64_t 
   float* a_row = row ? out->amax_row : nullptr;
   float* a_col = col ? out->amax_col : nullptr;
   const bool skip = flags & NVFP4_SKIP_AMAX;
-  CUtensorMap map;
+  CUtensorMap map, rmap;
   if (M > 0 && N > 0 && (st = x_map(x, dtype == NVFP4_BF16, M, N, &map)) != NVFP4_OK) return st;
+  if (M > 0 && N > 0 && (st = cached_map(rbits, 2, M, N, &rmap)) != NVFP4_OK) return st;
   if (!skip && launch_amax(x, dtype == NVFP4_BF16, M * N, a_row ? a_row : a_col, a_row ? a_col : nullptr, noop,
                            ctx) != cudaSuccess)
     return NVFP4_ERR_CUDA;
@@ -270,7 +276,7 @@ nvfp4_status quantize_sr(int mode, const void* x, int dtype, int64_t M, int64_t 
   a.rowwise = row;
   a.colwise = col;
   a.swizzled = (flags & NVFP4_SWIZZLED) != 0;
-  return from_cuda(launch_cast_sr(map, dtype == NVFP4_BF16, mode, a, rbits, /*pdl=*/!skip, ctx));
+  return from_cuda(launch_cast_sr(map, dtype == NVFP4_BF16, mode, a, rmap, /*pdl=*/!skip, ctx));
 }
 
 static_assert(NVFP4_MAX_GROUPS == kMaxGroups, "member table size");
@@ -360,6 +366,19 @@ cudaError_t make_x_tensor_map(CUtensorMap* map, const void* x, bool bf16, int64_
   CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                       const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_byte_tensor_map(CUtensorMap* map, const void* p, int64_t M, int64_t N) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)N};
+  cuuint32_t box[2] = {128u, 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(p), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

@@ -5,14 +5,15 @@
 // scales, the amax and the layouts are those of the plain cast; only the
 // rounding of each product p = x * r to E2M1 changes: between neighbouring
 // magnitudes lo <= |p| < hi the magnitude becomes hi iff
-// byte < 256 (|p| - lo) / (hi - lo).  |p| - lo is exact (lo <= |p| < 2 lo, or
-// lo = 0) and the step is a power of two, so the comparison is exact.
+// byte < 256 (|p| - lo) / (hi - lo), decided exactly by the carry form of
+// e2m1_sr (common.cuh): an offset made from the byte is added to the bits of
+// |p|, and the carry into the kept bit is the decision.
 //
 // The kernel is the two-pass cast (TMA-staged 128x128 tiles, persistent CTAs
 // in reverse tile order after the amax kernel) with the 8x8 sub-block mapping
-// of tile_ops.cuh; each thread also reads its sub-block's 64 random bytes
-// (eight 8-byte loads straight from global memory, read once for both
-// directions).
+// of tile_ops.cuh.  Each stage holds the x tile and, beside it, the tile's
+// 128 x 128 random bytes (one more TMA box on the same barrier); each thread
+// reads its sub-block's 64 bytes from there once, for both directions.
 #include <atomic>
 
 #include "common.cuh"
@@ -27,60 +28,81 @@ using namespace tile;
 
 constexpr int kSThreads = 256;
 
-// E2M1 code of p, stochastically rounded with the random byte rbf (an
-// integer 0..255 held as a float).  Branch-free (lanes hold different
-// values): the binade of |p| gives base (0, 2, 4) and the step (0.5, 1, 2);
-// t = (|p| - base) / step is exact, its integer part indexes the lower
-// neighbour and 256 times its fraction (exact) is compared with the byte.
-__device__ __forceinline__ uint32_t e2m1_sr(float p, float rbf) {
-  const float m = fabsf(p);
-  const bool b0 = m < 2.0f, b1 = m < 4.0f;
-  const float base = b0 ? 0.0f : (b1 ? 2.0f : 4.0f);
-  const float inv_step = b0 ? 2.0f : (b1 ? 1.0f : 0.5f);
-  const uint32_t cbase = b0 ? 0u : (b1 ? 4u : 6u);
-  const float t = __fmul_rn(__fsub_rn(m, base), inv_step);
-  const float ti = floorf(t);
-  const uint32_t up = rbf < __fmul_rn(__fsub_rn(t, ti), 256.0f) ? 1u : 0u;
-  // |p| >= 6 (t may be huge there; the conversion saturates) is 6
-  const uint32_t code = (m >= 6.0f) ? 7u : cbase + __float2uint_rz(ti) + up;
-  return code | ((__float_as_uint(p) >> 28) & 8u);
+// prmt.b32 with the selector's high bit per byte: that byte of the result is
+// the sign bit of the selected input byte, replicated.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
 }
 
-// Byte c (0..3) of w as a float: the bit pattern 2^23 + byte, minus 2^23.
-__device__ __forceinline__ float byte_f(uint32_t w, int c) {
-  return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)c)) - 8388608.0f;
-}
-__device__ __forceinline__ float byte_of(const uint2& w, int c) { return byte_f(c < 4 ? w.x : w.y, c & 3); }
-// Codes of row k of the sub-block times r (column c in nibble c), with the
-// row's eight random bytes.
+// Bit 4c + 3 set where column c of row k of the sub-block is negative: the
+// eight sign bits moved to where the codes of a row keep theirs.
 template <typename T>
-__device__ __forceinline__ uint32_t sr_row(const Sub<T>& s, int k, float r, const uint2& rb) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) w |= e2m1_sr(__fmul_rn(s.v(k, c), r), byte_of(rb, c)) << (4 * c);
-  return w;
-}
-// Codes of column c of the sub-block times r (row k in nibble k).
-template <typename T>
-__device__ __forceinline__ uint32_t sr_col(const Sub<T>& s, int c, float r, const uint2 (&rb)[8]) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) w |= e2m1_sr(__fmul_rn(s.v(k, c), r), byte_of(rb[k], c)) << (4 * k);
-  return w;
+__device__ __forceinline__ uint32_t sign_nibbles(const Sub<T>& s, int k) {
+  uint32_t even, odd;  // byte i: the sign of column 2i / 2i + 1, replicated
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t p = prmt(s.w[k][0], s.w[k][1], 0xFBD9u);  // columns 0, 2, 1, 3
+    const uint32_t q = prmt(s.w[k][2], s.w[k][3], 0xFBD9u);  // columns 4, 6, 5, 7
+    even = prmt(p, q, 0x5410u);
+    odd = prmt(p, q, 0x7632u);
+  } else {
+    even = prmt(prmt(s.w[k][0], s.w[k][2], 0xFBFBu), prmt(s.w[k][4], s.w[k][6], 0xFBFBu), 0x5410u);
+    odd = prmt(prmt(s.w[k][1], s.w[k][3], 0xFBFBu), prmt(s.w[k][5], s.w[k][7], 0xFBFBu), 0x5410u);
+  }
+  return ((even & 0x0F0F0F0Fu) | (odd & 0xF0F0F0F0u)) & 0x88888888u;
 }
 
-__device__ __forceinline__ uint2 ld_nc_v2(const uint8_t* p) {
+// Packing eight codes-plus-252 four bits apart and subtracting this once
+// leaves the eight codes (the sums wrap mod 2^32, which the subtraction
+// undoes exactly).
+constexpr uint32_t kCode252x8 = 252u * 0x11111111u;
+
+// Codes of row k of the sub-block (column c in nibble c) times the factor
+// of column c, fr[c] (1D column-wise: the column's factor; otherwise one
+// factor for the row), with the row's random bytes (complemented: nrb).
+template <typename T>
+__device__ __forceinline__ uint32_t sr_row_word(const Sub<T>& s, int k, const float (&f)[8], const uint2& nrb,
+                                                uint32_t sgn) {
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    acc += sr_code252(__fmul_rn(fabsf(s.v(k, c)), f[c]), sr_offset_nw(c < 4 ? nrb.x : nrb.y, c & 3)) << (4 * c);
+  return (acc - kCode252x8) | sgn;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
+}
+
+// A stage: the x tile, then the tile's random bytes (128 rows of 128 bytes,
+// 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)).
+constexpr uint32_t kRbTileBytes = 128 * 128;
+template <typename T>
+__host__ __device__ constexpr uint32_t sr_stage_bytes() {
+  return (uint32_t)tile_bytes<T>() + kRbTileBytes;
+}
+// Stages per CTA: two (BF16: two CTAs of 2 x 48 KB per SM; FP32: one CTA of
+// 2 x 80 KB).
+template <typename T, int MODE>
+__host__ __device__ constexpr int sr_stages() {
+  return 2;
+}
+// stages | 2 encode-factor tables | 2 x 2 staged scale regions | barriers | flag
+template <typename T, int MODE>
+__host__ __device__ constexpr size_t sr_smem_bytes() {
+  return 1024 + (size_t)sr_stages<T, MODE>() * sr_stage_bytes<T>() + 2 * 128 * 4 + 4 * kScRegion +
+         8 * sr_stages<T, MODE>() + 16;
 }
 
 // The sub-block pass of tile_ops.cuh (same mapping, scales, staging and
 // stores) with stochastically rounded codes.
 template <typename T, int MODE, int kDirs, bool kInterior>
 __device__ __forceinline__ void sr_pass(uint32_t stage, const float* rtab_row, const float* rtab_col,
-                                        uint32_t sc_row, uint32_t sc_col, const CastArgs& a, const uint8_t* rbits,
-                                        int64_t r0, int64_t c0, float g_row, float g_col, int warp) {
+                                        uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0, int64_t c0,
+                                        float g_row, float g_col, int warp) {
   constexpr bool kRow = (kDirs & 1) != 0, kCol = (kDirs & 2) != 0;
   const int lane = threadIdx.x & 31;
   const int bx = warp & 1, q = warp >> 1, j = lane & 7, i = lane >> 3;
@@ -90,12 +112,17 @@ __device__ __forceinline__ void sr_pass(uint32_t stage, const float* rtab_row, c
   load_sub<T>(stage, bx, trow, j, s);
 
   const int64_t M = a.M, N = a.N, y0 = r0 + trow, x0 = c0 + tcol;
-  // the sub-block's random bytes: row k at rb[k], column c in byte c
+  // the sub-block's random bytes, complemented (the encoder's form): row k
+  // at rb[k], column c in byte c; outside x they are the zero fill, unused
   uint2 rb[8];
-  const uint8_t* prb = rbits + y0 * N + x0;
+  const uint32_t rstage = stage + (uint32_t)tile_bytes<T>();
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    rb[k] = (kInterior || (y0 + k < M && x0 < N)) ? ld_nc_v2(prb + k * N) : make_uint2(0u, 0u);
+  for (int k = 0; k < 8; ++k) {
+    const int r = trow + k;
+    rb[k] = lds64(rstage + (uint32_t)(r * 128 + ((((tcol >> 4) ^ (r & 7)) << 4) | (tcol & 8))));
+    rb[k].x = ~rb[k].x;
+    rb[k].y = ~rb[k].y;
+  }
 
   const int64_t srow = N / 2, scol = M / 2;
   uint8_t* prow = kRow ? a.data_row + y0 * srow + x0 / 2 : nullptr;
@@ -124,30 +151,36 @@ __device__ __forceinline__ void sr_pass(uint32_t stage, const float* rtab_row, c
   };
   const bool stage_row = (j & 1) == 0, stage_col = (i & 1) == 0;
 
+  // Every code of a row is made in row order, the column-wise ones too (with
+  // their columns' factors), and the column-wise words are transposed at the
+  // end; the signs of a row serve both directions.
+  uint32_t wc[8];
   if constexpr (MODE == kCast2D) {
     const float m = tile_max<T>(s);
     const uint32_t sr = block_scale(m, g_row);
     const uint32_t sc = (g_col == g_row) ? sr : block_scale(m, g_col);
     const float rr = rtab_row[sr], rc = rtab_col[sc];
-    uint32_t wc[8];
+    float fr[8], fc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      fr[c] = kRow ? rr : rc;
+      fc[c] = rc;
+    }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t wr = sr_row(s, k, kRow ? rr : rc, rb[k]);
+      const uint32_t sgn = sign_nibbles(s, k);
+      const uint32_t wr = sr_row_word(s, k, fr, rb[k], sgn);
       if (kRow) put_row(k, wr);
       // an element keeps its byte in both directions, so with one factor the
       // column codes are the transposed row codes
-      if (kCol) wc[k] = (!kRow || rc == rr) ? wr : sr_row(s, k, rc, rb[k]);
-    }
-    if (kCol) {
-      transpose_nibbles8x8(wc);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) put_col(c, wc[c]);
+      if (kCol) wc[k] = (!kRow || rc == rr) ? wr : sr_row_word(s, k, fc, rb[k], sgn);
     }
     if (stage_row && stage_col) {
       if (kRow) sts_u8(sc_row + (uint32_t)((trow >> 4) * 8 + (tcol >> 4)), sr);
       if (kCol) sts_u8(sc_col + (uint32_t)((tcol >> 4) * 8 + (trow >> 4)), sc);
     }
   } else {
+    float fr[8], fc[8];  // factors of the sub-block's rows / columns
     if (kRow) {
       uint32_t packed[2] = {0u, 0u};
 #pragma unroll
@@ -162,8 +195,8 @@ __device__ __forceinline__ void sr_pass(uint32_t stage, const float* rtab_row, c
           m1 = row_max_f32(s, 2 * t + 1);
         }
         const uint32_t s01 = block_scale2(m0, m1, g_row), s0 = s01 & 0xFFu, s1 = s01 >> 8;
-        put_row(2 * t, sr_row(s, 2 * t, rtab_row[s0], rb[2 * t]));
-        put_row(2 * t + 1, sr_row(s, 2 * t + 1, rtab_row[s1], rb[2 * t + 1]));
+        fr[2 * t] = rtab_row[s0];
+        fr[2 * t + 1] = rtab_row[s1];
         packed[t >> 1] |= (s0 | (s1 << 8)) << (16 * (t & 1));
       }
       if (stage_row) sts_v2(sc_row + (uint32_t)((tcol >> 4) * kScPitchRow + trow), packed[0], packed[1]);
@@ -182,36 +215,52 @@ __device__ __forceinline__ void sr_pass(uint32_t stage, const float* rtab_row, c
           m1 = col_max_f32(s, 2 * p + 1);
         }
         const uint32_t s01 = block_scale2(m0, m1, g_col), s0 = s01 & 0xFFu, s1 = s01 >> 8;
-        put_col(2 * p, sr_col(s, 2 * p, rtab_col[s0], rb));
-        put_col(2 * p + 1, sr_col(s, 2 * p + 1, rtab_col[s1], rb));
+        fc[2 * p] = rtab_col[s0];
+        fc[2 * p + 1] = rtab_col[s1];
         packed[p >> 1] |= (s0 | (s1 << 8)) << (16 * (p & 1));
       }
       if (stage_col) sts_v2(sc_col + (uint32_t)((trow >> 4) * kScPitchCol + tcol), packed[0], packed[1]);
     }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t sgn = sign_nibbles(s, k);
+      if (kRow) {
+        float f[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) f[c] = fr[k];
+        put_row(k, sr_row_word(s, k, f, rb[k], sgn));
+      }
+      if (kCol) wc[k] = sr_row_word(s, k, fc, rb[k], sgn);
+    }
+  }
+  if (kCol) {
+    transpose_nibbles8x8(wc);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) put_col(c, wc[c]);
   }
 }
 
 template <typename T, int MODE>
 __device__ __forceinline__ void sr_pass_any(uint32_t stage, const float* rtab_row, const float* rtab_col,
-                                            uint32_t sc_row, uint32_t sc_col, const CastArgs& a,
-                                            const uint8_t* rbits, int64_t r0, int64_t c0, float g_row, float g_col,
-                                            bool do_row, bool do_col, int warp) {
+                                            uint32_t sc_row, uint32_t sc_col, const CastArgs& a, int64_t r0,
+                                            int64_t c0, float g_row, float g_col, bool do_row, bool do_col,
+                                            int warp) {
   const bool interior = (r0 + kTile <= a.M) && (c0 + kTile <= a.N);
   if (do_row && do_col) {
     if (interior)
-      sr_pass<T, MODE, 3, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, rbits, r0, c0, g_row, g_col, warp);
+      sr_pass<T, MODE, 3, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
     else
-      sr_pass<T, MODE, 3, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, rbits, r0, c0, g_row, g_col, warp);
+      sr_pass<T, MODE, 3, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
   } else if (do_row) {
     if (interior)
-      sr_pass<T, MODE, 1, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, rbits, r0, c0, g_row, g_col, warp);
+      sr_pass<T, MODE, 1, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
     else
-      sr_pass<T, MODE, 1, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, rbits, r0, c0, g_row, g_col, warp);
+      sr_pass<T, MODE, 1, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
   } else if (do_col) {
     if (interior)
-      sr_pass<T, MODE, 2, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, rbits, r0, c0, g_row, g_col, warp);
+      sr_pass<T, MODE, 2, true>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
     else
-      sr_pass<T, MODE, 2, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, rbits, r0, c0, g_row, g_col, warp);
+      sr_pass<T, MODE, 2, false>(stage, rtab_row, rtab_col, sc_row, sc_col, a, r0, c0, g_row, g_col, warp);
   }
 }
 
@@ -225,35 +274,36 @@ struct SSmem {
   int* abort_flag;
 };
 
-template <typename T>
+template <typename T, int MODE>
 __device__ __forceinline__ SSmem scarve(uint8_t* raw) {
   SSmem s;
   uint8_t* p = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
   s.stages = p;
-  p += (size_t)TileCfg<T>::kStages * tile_bytes<T>();
+  p += (size_t)sr_stages<T, MODE>() * sr_stage_bytes<T>();
   s.rtab_row = reinterpret_cast<float*>(p);
   s.rtab_col = s.rtab_row + 128;
   s.sc_row = reinterpret_cast<uint8_t*>(s.rtab_col + 128);
   s.sc_col = s.sc_row + 2 * kScRegion;
   s.bars = reinterpret_cast<uint64_t*>(s.sc_col + 2 * kScRegion);
-  s.abort_flag = reinterpret_cast<int*>(s.bars + TileCfg<T>::kStages);
+  s.abort_flag = reinterpret_cast<int*>(s.bars + sr_stages<T, MODE>());
   return s;
 }
 
-// CTAs per SM the register budget is set for: two for BF16 2D (128
-// registers, no spills), else one (the 1D encoder of both directions keeps
-// more values live; a two-CTA budget spills).
+// CTAs per SM the register budget is set for: two for BF16 (128 registers,
+// no spills), one for FP32.
 template <typename T, int MODE>
 constexpr int sr_min_blocks() {
-  return (MODE == kCast2D && sizeof(T) == 2) ? 2 : 1;
+  return sizeof(T) == 2 ? 2 : 1;
 }
 
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kSThreads, sr_min_blocks<T, MODE>())
-    sr_cast_kernel(const __grid_constant__ CUtensorMap tmap, const CastArgs a, const uint8_t* __restrict__ rbits) {
+    sr_cast_kernel(const __grid_constant__ CUtensorMap tmap, const CastArgs a,
+                   const __grid_constant__ CUtensorMap rmap) {
   using C = TileCfg<T>;
+  constexpr int S = sr_stages<T, MODE>();
   extern __shared__ uint8_t smem_raw[];
-  const SSmem sm = scarve<T>(smem_raw);
+  const SSmem sm = scarve<T, MODE>(smem_raw);
   const int tid = threadIdx.x;
   if (a.noop != nullptr && *a.noop == 1.0f) return;
 
@@ -263,25 +313,27 @@ __global__ void __launch_bounds__(kSThreads, sr_min_blocks<T, MODE>())
   auto tile_of = [&](int k) { return num_tiles - 1 - (bid + k * nb); };
 
   if (tid == 0) {
-    for (int s = 0; s < C::kStages; ++s) mbar_init(&sm.bars[s], 1);
+    for (int s = 0; s < S; ++s) mbar_init(&sm.bars[s], 1);
     *sm.abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmap);
+    tma_prefetch_desc(&rmap);
   }
   __syncthreads();
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int k) {
     const int t = tile_of(k);
     const int tr = t / a.tiles_n, tc = t - tr * a.tiles_n;
-    uint8_t* dst = sm.stages + (size_t)(k % C::kStages) * tile_bytes<T>();
-    uint64_t* bar = &sm.bars[k % C::kStages];
-    mbar_arrive_expect_tx(bar, tile_bytes<T>());
+    uint8_t* dst = sm.stages + (size_t)(k % S) * sr_stage_bytes<T>();
+    uint64_t* bar = &sm.bars[k % S];
+    mbar_arrive_expect_tx(bar, sr_stage_bytes<T>());
 #pragma unroll
     for (int b = 0; b < C::kBoxes; ++b)
       tma_load_2d(dst + b * kBoxBytes, &tmap, tc * kTile + b * C::kBoxCols, tr * kTile, bar, policy);
+    tma_load_2d(dst + tile_bytes<T>(), &rmap, tc * kTile, tr * kTile, bar, policy);
   };
   if (tid == 0)
-    for (int k = 0; k < C::kStages && k < my_count; ++k) issue(k);
+    for (int k = 0; k < S && k < my_count; ++k) issue(k);
 
   grid_dependency_wait();  // the amax written by the preceding kernel is visible
   const float g_row = global_encode_scale(a.amax_row ? *a.amax_row : 0.0f);
@@ -295,22 +347,21 @@ __global__ void __launch_bounds__(kSThreads, sr_min_blocks<T, MODE>())
   const bool do_row = a.rowwise != 0, do_col = a.colwise != 0;
   int k = 0;
   for (; k < my_count; ++k) {
-    const int s = k % C::kStages;
-    const bool ok =
-        __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.bars[s], (uint32_t)((k / C::kStages) & 1), a.status));
+    const int s = k % S;
+    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.bars[s], (uint32_t)((k / S) & 1), a.status));
     if (!ok) *sm.abort_flag = 1;
     const int t = tile_of(k);
     const int tr = t / a.tiles_n, tc = t - tr * a.tiles_n;
     const int64_t r0 = (int64_t)tr * kTile, c0 = (int64_t)tc * kTile;
-    const uint8_t* st = sm.stages + (size_t)s * tile_bytes<T>();
+    const uint8_t* st = sm.stages + (size_t)s * sr_stage_bytes<T>();
     const int parity = k & 1;
     if (ok)
       sr_pass_any<T, MODE>(smem_u32(st), sm.rtab_row, sm.rtab_col, smem_u32(sm.sc_row + parity * kScRegion),
-                           smem_u32(sm.sc_col + parity * kScRegion), a, rbits, r0, c0, g_row, g_col, do_row, do_col,
+                           smem_u32(sm.sc_col + parity * kScRegion), a, r0, c0, g_row, g_col, do_row, do_col,
                            tid >> 5);
     __syncthreads();  // stage s fully read; this tile's scales staged
     if (*sm.abort_flag) break;
-    if (tid == 0 && k + C::kStages < my_count) issue(k + C::kStages);
+    if (tid == 0 && k + S < my_count) issue(k + S);
     if (tid < 128) {
       if (do_row)
         store_scale_tile<MODE, false>(sm.sc_row + parity * kScRegion, a.scale_row, r0, c0 / 16, a.M, a.N / 16,
@@ -323,15 +374,15 @@ __global__ void __launch_bounds__(kSThreads, sr_min_blocks<T, MODE>())
   if (k < my_count && tid == 0) {
     // A wait ran out: wait (bounded) for this CTA's copies still in flight
     // before the shared memory is released.
-    const int issued = (k + C::kStages < my_count) ? k + C::kStages : my_count;
-    for (int jj = k; jj < issued; ++jj)
-      mbar_wait_bounded(&sm.bars[jj % C::kStages], (uint32_t)((jj / C::kStages) & 1), a.status);
+    const int issued = (k + S < my_count) ? k + S : my_count;
+    for (int jj = k; jj < issued; ++jj) mbar_wait_bounded(&sm.bars[jj % S], (uint32_t)((jj / S) & 1), a.status);
   }
 }
 
 template <typename T, int MODE>
-cudaError_t launch_t(const CUtensorMap& map, const CastArgs& a, const uint8_t* rbits, bool pdl,
+cudaError_t launch_t(const CUtensorMap& map, const CastArgs& a, const CUtensorMap& rmap, bool pdl,
                      const LaunchCtx& ctx) {
+  constexpr size_t kSmem = sr_smem_bytes<T, MODE>();
   auto fn = sr_cast_kernel<T, MODE>;
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
@@ -339,37 +390,36 @@ cudaError_t launch_t(const CUtensorMap& map, const CastArgs& a, const uint8_t* r
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(attr_set.load() & bit)) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<T>());
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
   // the CTAs per SM that fit (registers, shared memory), at most two
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessorWithFlags(&per_sm, fn, kSThreads, smem_bytes<T>(),
-                                                             cudaOccupancyDefault);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessorWithFlags(&per_sm, fn, kSThreads, kSmem, cudaOccupancyDefault);
   if (e != cudaSuccess) return e;
   const int cap = ctx.num_sms * (per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm));
   const int grid = a.num_tiles < cap ? a.num_tiles : cap;
   if (grid == 0) return cudaSuccess;
-  void* args[] = {(void*)&map, (void*)&a, (void*)&rbits};
-  if (pdl) return launch_pdl((const void*)fn, dim3(grid), dim3(kSThreads), smem_bytes<T>(), ctx.stream, args);
-  fn<<<grid, kSThreads, smem_bytes<T>(), ctx.stream>>>(map, a, rbits);
+  void* args[] = {(void*)&map, (void*)&a, (void*)&rmap};
+  if (pdl) return launch_pdl((const void*)fn, dim3(grid), dim3(kSThreads), kSmem, ctx.stream, args);
+  fn<<<grid, kSThreads, kSmem, ctx.stream>>>(map, a, rmap);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_cast_sr(const CUtensorMap& map, bool bf16, int mode, CastArgs args, const uint8_t* rbits,
+cudaError_t launch_cast_sr(const CUtensorMap& map, bool bf16, int mode, CastArgs args, const CUtensorMap& rmap,
                            bool pdl, const LaunchCtx& ctx) {
   const int64_t tiles_m = (args.M + kTile - 1) / kTile, tiles_n = (args.N + kTile - 1) / kTile;
   args.tiles_n = (int)tiles_n;
   args.num_tiles = (int)(tiles_m * tiles_n);
   if (bf16) {
-    if (mode == kCast1D) return launch_t<uint16_t, kCast1D>(map, args, rbits, pdl, ctx);
-    return launch_t<uint16_t, kCast2D>(map, args, rbits, pdl, ctx);
+    if (mode == kCast1D) return launch_t<uint16_t, kCast1D>(map, args, rmap, pdl, ctx);
+    return launch_t<uint16_t, kCast2D>(map, args, rmap, pdl, ctx);
   }
-  if (mode == kCast1D) return launch_t<float, kCast1D>(map, args, rbits, pdl, ctx);
-  return launch_t<float, kCast2D>(map, args, rbits, pdl, ctx);
+  if (mode == kCast1D) return launch_t<float, kCast1D>(map, args, rmap, pdl, ctx);
+  return launch_t<float, kCast2D>(map, args, rmap, pdl, ctx);
 }
 
 }  // namespace nvfp4

@@ -1,5 +1,6 @@
 // gpu_selftest.cu -- test-only kernels that run the library's device helpers
-// (hardware E2M1 / E4M3 / BF16 conversions, the division by 6, the bounded
+// (hardware E2M1 / E4M3 / BF16 conversions, the stochastic-rounding E2M1
+// encoder, the division by 6, the bounded
 // mbarrier wait) on arbitrary inputs, so the tests can compare them with the
 // oracle exhaustively.  Built by the GPU tests; never part of libnvfp4.
 #include "common.cuh"
@@ -14,6 +15,11 @@ __global__ void e2m1_kernel(const float* in, uint8_t* out, int64_t n8) {
     const uint32_t w = e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
     for (int k = 0; k < 8; ++k) out[8 * i + k] = (w >> (4 * k)) & 0xFu;
   }
+}
+
+__global__ void e2m1_sr_kernel(const float* in, const uint8_t* rb, uint8_t* out, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = (uint8_t)e2m1_sr(in[i], sr_offset(rb[i]));
 }
 
 __global__ void e4m3_kernel(const float* in, uint8_t* out, int64_t n) {
@@ -58,6 +64,11 @@ extern "C" {
 
 int selftest_e2m1(const float* in, uint8_t* out, int64_t n) {
   e2m1_kernel<<<1024, 256>>>(in, out, n / 8);
+  return (int)cudaDeviceSynchronize();
+}
+
+int selftest_e2m1_sr(const float* in, const uint8_t* rb, uint8_t* out, int64_t n) {
+  e2m1_sr_kernel<<<1024, 256>>>(in, rb, out, n);
   return (int)cudaDeviceSynchronize();
 }
 

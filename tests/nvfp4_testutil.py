@@ -29,6 +29,7 @@ def build_selftest() -> ctypes.CDLL:
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     L.selftest_e2m1.argtypes = [vp, vp, i64]
     L.selftest_e4m3.argtypes = [vp, vp, i64]
+    L.selftest_e2m1_sr.argtypes = [vp, vp, vp, i64]
     L.selftest_bf16.argtypes = [vp, vp, i64]
     L.selftest_div6.argtypes = [ctypes.c_uint32, ctypes.c_uint32, vp, vp]
     L.selftest_wait_timeout.argtypes = [vp, ctypes.c_longlong, vp]

@@ -1,5 +1,6 @@
 """The kernels' number-format building blocks on the GPU, compared with the
-oracle exhaustively: hardware E2M1 / E4M3 / BF16 conversions, the FMA-
+oracle exhaustively: hardware E2M1 / E4M3 / BF16 conversions, the
+stochastic-rounding E2M1 encoder, the FMA-
 corrected division by 6 against IEEE division over every positive FP32
 value, and the bounded mbarrier wait giving up on a barrier nobody signals."""
 import ctypes
@@ -48,6 +49,36 @@ def test_e2m1_cvt_matches_oracle(st, oracle_mod):
     ref = oracle_mod.encode_array(vals, "e2m1")
     bad = np.nonzero(got != ref)[0]
     assert bad.size == 0, f"{bad.size} mismatches, e.g. {vals[bad[:5]]} -> gpu {got[bad[:5]]} oracle {ref[bad[:5]]}"
+
+
+def test_e2m1_sr_encoder_matches_oracle(st, oracle_mod):
+    """The stochastic-rounding encoder (carry form) against the oracle's
+    rule: every finite BF16 value with every byte, the neighbourhoods of the
+    points lo + b/256 (hi - lo) of every interval and byte (where a fraction
+    just above b/256 must still round up: values whose low bits the carry
+    form's truncation drops), and random FP32 values with random bytes."""
+    bf = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    bf = bf[np.isfinite(bf)]
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+    pts = np.array([lo + (hi - lo) * b / 256 for lo, hi in zip(mags[:-1], mags[1:]) for b in range(256)])
+    near = _neighbourhoods(pts[pts > 0], 3)
+    rng = np.random.default_rng(3)
+    rnd = (rng.choice([-1.0, 1.0], 1 << 22) * np.exp2(rng.uniform(-30, 4, 1 << 22))).astype(np.float32)
+    special = np.array([0.0, -0.0, 1e-45, -1e-45, 1e-38, 6.0, -6.0, 7.9, 3e38, -3e38, np.inf, -np.inf], np.float32)
+    cases = [(np.repeat(bf, 256), np.tile(np.arange(256, dtype=np.uint8), bf.size)),
+             (np.repeat(near, 256), np.tile(np.arange(256, dtype=np.uint8), near.size)),
+             (rnd, rng.integers(0, 256, rnd.size).astype(np.uint8)),
+             (np.repeat(special, 256), np.tile(np.arange(256, dtype=np.uint8), special.size))]
+    for vals, rb in cases:
+        x = torch.from_numpy(np.ascontiguousarray(vals, np.float32)).cuda()
+        r = torch.from_numpy(np.ascontiguousarray(rb, np.uint8)).cuda()
+        out = torch.empty(x.numel(), dtype=torch.uint8, device="cuda")
+        assert st.selftest_e2m1_sr(x.data_ptr(), r.data_ptr(), out.data_ptr(), x.numel()) == 0
+        got = out.cpu().numpy()
+        ref = oracle_mod.e2m1_sr_array(vals, rb)
+        bad = np.nonzero(got != ref)[0]
+        assert bad.size == 0, (f"{bad.size} of {vals.size} differ, e.g. {vals[bad[:5]]} bytes {rb[bad[:5]]} -> "
+                               f"gpu {got[bad[:5]]} oracle {ref[bad[:5]]}")
 
 
 def test_e4m3_cvt_matches_oracle(st, oracle_mod):
