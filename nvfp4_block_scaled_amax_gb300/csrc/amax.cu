@@ -12,8 +12,6 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kAmaxThreads = 256;
-
 __global__ void amax_zero_kernel(float* a, float* b, const float* noop) {
   grid_launch_dependents();
   if (noop != nullptr && *noop == 1.0f) return;
@@ -50,72 +48,109 @@ __device__ __forceinline__ void publish_max(float m, float* a, float* b) {
   if (b != nullptr) atomicMax(reinterpret_cast<int*>(b), __float_as_int(m));
 }
 
-// max|x| over n elements; x is 16-byte aligned.  nvec 16-byte vectors are
-// read by the grid-stride loop in batches of kUnroll independent loads per
-// thread (the last batch predicated, so no load waits behind another); one
-// resident wave of CTAs keeps ~128 KB of reads in flight per SM.  The last
-// n - nvec*epv elements are read by block 0.
-constexpr int kUnroll = 8;
+// max|x| over n elements; x is 16-byte aligned.  One persistent CTA per SM
+// streams 32 KB chunks of x (chunk b + k G for CTA b of G) through a ring of
+// kAmaxStages shared-memory stages with bulk copies, several chunks in flight
+// per SM; each chunk is folded by the CTA's threads (16-byte reads,
+// consecutive threads on consecutive vectors), then refilled.  The last
+// (n * element size) mod 16 bytes are read by block 0.
+constexpr int kAmaxThreads = 512, kAmaxStages = 4;
+constexpr uint32_t kAmaxChunk = 32768;
+constexpr size_t kAmaxSmem = (size_t)kAmaxStages * kAmaxChunk + 128;
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kAmaxThreads, 4) amax_reduce_kernel(const void* __restrict__ x, int64_t n,
-                                                                      float* a, float* b, const float* noop) {
+__global__ void __launch_bounds__(kAmaxThreads, 1) amax_reduce_kernel(const uint8_t* __restrict__ x, int64_t n,
+                                                                      float* a, float* b, const float* noop,
+                                                                      unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kAmaxStages];
   __shared__ float red[kAmaxThreads / 32];
+  __shared__ int failed;
   grid_launch_dependents();
   if (noop != nullptr && *noop == 1.0f) return;
-  constexpr int kEpv = kBF16 ? 8 : 4;
-  const uint4* xv = static_cast<const uint4*>(x);
-  const int64_t nvec = n / kEpv;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  float m = 0.0f;
-  if constexpr (kBF16) {
-    uint32_t acc0 = 0, acc1 = 0;
-    auto fold = [&](const uint4& v) {
-      uint32_t t0, t1;
-      asm("max.bf16x2 %0, %1, %2;" : "=r"(t0) : "r"(v.x & 0x7FFF7FFFu), "r"(v.y & 0x7FFF7FFFu));
-      asm("max.bf16x2 %0, %1, %2;" : "=r"(t1) : "r"(v.z & 0x7FFF7FFFu), "r"(v.w & 0x7FFF7FFFu));
-      asm("max.bf16x2 %0, %0, %1;" : "+r"(acc0) : "r"(t0));
-      asm("max.bf16x2 %0, %0, %1;" : "+r"(acc1) : "r"(t1));
-    };
-    for (; i < nvec; i += kUnroll * stride) {
-      uint4 v[kUnroll];
+  constexpr int kEb = kBF16 ? 2 : 4;
+  const uint32_t stages = (smem_u32(smem_raw) + 127u) & ~127u;
+  const int tid = threadIdx.x, G = gridDim.x, bid = blockIdx.x;
+  const int64_t main_bytes = (n * kEb) & ~(int64_t)15;
+  const int64_t nchunks = (main_bytes + kAmaxChunk - 1) / kAmaxChunk;
+  const int my = bid < nchunks ? (int)((nchunks - 1 - bid) / G + 1) : 0;
+  auto chunk_bytes = [&](int k) {
+    const int64_t left = main_bytes - (bid + (int64_t)k * G) * (int64_t)kAmaxChunk;
+    return (uint32_t)(left < (int64_t)kAmaxChunk ? left : (int64_t)kAmaxChunk);
+  };
+  auto issue = [&](int k) {
+    const int s = k % kAmaxStages;
+    const uint32_t sz = chunk_bytes(k);
+    mbar_arrive_expect_tx(&full[s], sz);
+    bulk_load(stages + (uint32_t)s * kAmaxChunk, x + (bid + (int64_t)k * G) * (int64_t)kAmaxChunk, sz, &full[s]);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kAmaxStages; ++s) mbar_init(&full[s], 1);
+    failed = 0;
+    fence_mbar_init();
+    for (int k = 0; k < kAmaxStages && k < my; ++k) issue(k);
+  }
+  __syncthreads();
+  uint32_t acc0 = 0, acc1 = 0;  // BF16: packed maxima of |x|
+  float m0 = 0.0f, m1 = 0.0f;   // FP32
+  int k = 0;
+  for (; k < my; ++k) {
+    const int s = k % kAmaxStages;
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((k / kAmaxStages) & 1), status);
+    if (__syncthreads_or(!ok)) break;
+    const uint32_t sz = chunk_bytes(k), base = stages + (uint32_t)s * kAmaxChunk;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        v[u] = (i + u * stride < nvec) ? ld_stream(xv + i + u * stride) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) fold(v[u]);
+    for (int q = 0; q < (int)(kAmaxChunk / 16 / kAmaxThreads); ++q) {
+      const uint32_t off = (uint32_t)(q * kAmaxThreads + tid) * 16u;
+      if (off < sz) {
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(base + off));
+        if constexpr (kBF16) {
+          uint32_t t0, t1;
+          asm("max.bf16x2 %0, %1, %2;" : "=r"(t0) : "r"(v.x & 0x7FFF7FFFu), "r"(v.y & 0x7FFF7FFFu));
+          asm("max.bf16x2 %0, %1, %2;" : "=r"(t1) : "r"(v.z & 0x7FFF7FFFu), "r"(v.w & 0x7FFF7FFFu));
+          asm("max.bf16x2 %0, %0, %1;" : "+r"(acc0) : "r"(t0));
+          asm("max.bf16x2 %0, %0, %1;" : "+r"(acc1) : "r"(t1));
+        } else {
+          m0 = fmaxf(m0, fmaxf(fabsf(__uint_as_float(v.x)), fabsf(__uint_as_float(v.y))));
+          m1 = fmaxf(m1, fmaxf(fabsf(__uint_as_float(v.z)), fabsf(__uint_as_float(v.w))));
+        }
+      }
     }
+    __syncthreads();  // stage s read by every thread
+    if (tid == 0 && k + kAmaxStages < my) issue(k + kAmaxStages);
+  }
+  if (k < my) {
+    // A wait ran out (status recorded): let the copies still in flight land,
+    // bounded, before the shared memory is released; publish nothing.
+    if (tid == 0) {
+      const int issued = k + kAmaxStages < my ? k + kAmaxStages : my;
+      for (int jj = k; jj < issued; ++jj)
+        mbar_wait_bounded(&full[jj % kAmaxStages], (uint32_t)((jj / kAmaxStages) & 1), status);
+    }
+    return;
+  }
+  float m;
+  if constexpr (kBF16) {
     uint32_t acc;
     asm("max.bf16x2 %0, %1, %2;" : "=r"(acc) : "r"(acc0), "r"(acc1));
     m = bf16x2_hmax_to_f32(acc);
-    if (blockIdx.x == 0) {
-      const uint16_t* xs = static_cast<const uint16_t*>(x);
-      for (int64_t j = nvec * kEpv + threadIdx.x; j < n; j += blockDim.x)
+    if (bid == 0) {
+      const uint16_t* xs = reinterpret_cast<const uint16_t*>(x);
+      for (int64_t j = main_bytes / kEb + tid; j < n; j += kAmaxThreads)
         m = fmaxf(m, fabsf(__uint_as_float((uint32_t)xs[j] << 16)));
     }
   } else {
-    float m0 = 0.0f, m1 = 0.0f;
-    auto fold = [&](const uint4& v) {
-      m0 = fmaxf(m0, fmaxf(fabsf(__uint_as_float(v.x)), fabsf(__uint_as_float(v.y))));
-      m1 = fmaxf(m1, fmaxf(fabsf(__uint_as_float(v.z)), fabsf(__uint_as_float(v.w))));
-    };
-    for (; i < nvec; i += kUnroll * stride) {
-      uint4 v[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        v[u] = (i + u * stride < nvec) ? ld_stream(xv + i + u * stride) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) fold(v[u]);
-    }
     m = fmaxf(m0, m1);
-    if (blockIdx.x == 0) {
-      const float* xs = static_cast<const float*>(x);
-      for (int64_t j = nvec * kEpv + threadIdx.x; j < n; j += blockDim.x) m = fmaxf(m, fabsf(xs[j]));
+    if (bid == 0) {
+      const float* xs = reinterpret_cast<const float*>(x);
+      for (int64_t j = main_bytes / kEb + tid; j < n; j += kAmaxThreads) m = fmaxf(m, fabsf(xs[j]));
     }
   }
   m = block_max(m, red);
-  if (threadIdx.x == 0) publish_max(m, a, b);
+  if (tid == 0) publish_max(m, a, b);
 }
 
 constexpr int kRhtAmaxThreads = 256;
@@ -187,22 +222,23 @@ cudaError_t launch_amax(const void* x, bool bf16, int64_t n, float* amax_a, floa
   amax_zero_kernel<<<1, 1, 0, ctx.stream>>>(amax_a, amax_b, noop);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int epv = bf16 ? 8 : 4;
-  const int64_t nvec = n / epv;
   const void* fn = bf16 ? (const void*)amax_reduce_kernel<true> : (const void*)amax_reduce_kernel<false>;
-  // One resident wave of CTAs; each walks the tensor with a grid stride.
-  static std::atomic<int> occ[2] = {0, 0};  // CTAs per SM, same on every GB300
-  int per_sm = occ[bf16].load();
-  if (per_sm == 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kAmaxThreads, 0);
-    if (e != cudaSuccess) return e;
-    occ[bf16].store(per_sm);
+  static std::atomic<uint64_t> attr_set[2] = {0, 0};  // per kernel, bit per device
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_set[bf16].load() & bit)) {
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAmaxSmem)) != cudaSuccess)
+      return e;
+    attr_set[bf16].fetch_or(bit);
   }
-  int64_t want = (nvec + kAmaxThreads * kUnroll - 1) / (kAmaxThreads * kUnroll);
-  int64_t cap = (int64_t)ctx.num_sms * (per_sm > 0 ? per_sm : 1);
-  int grid = (int)(want < 1 ? 1 : (want > cap ? cap : want));
-  void* args[] = {(void*)&x, (void*)&n, (void*)&amax_a, (void*)&amax_b, (void*)&noop};
-  return launch_pdl(fn, dim3(grid), dim3(kAmaxThreads), 0, ctx.stream, args);
+  // one persistent CTA per SM (fewer if x has fewer 32 KB chunks)
+  const int64_t chunks = ((n * (bf16 ? 2 : 4)) / 16 * 16 + kAmaxChunk - 1) / kAmaxChunk;
+  const int grid = (int)(chunks < 1 ? 1 : (chunks > ctx.num_sms ? ctx.num_sms : chunks));
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  unsigned* status = ctx.status;
+  void* args[] = {(void*)&xb, (void*)&n, (void*)&amax_a, (void*)&amax_b, (void*)&noop, (void*)&status};
+  return launch_pdl(fn, dim3(grid), dim3(kAmaxThreads), kAmaxSmem, ctx.stream, args);
 }
 
 cudaError_t launch_rht_amax(const uint16_t* x, int64_t M, int64_t N, uint32_t sign_mask, float* amax_row,

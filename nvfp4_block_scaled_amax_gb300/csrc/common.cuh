@@ -109,9 +109,9 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
 // y > n for an integer n).  max(v, w) is v below 1 and w from 1 up.  Every
 // step is exact; sr_code252 returns the code plus 252 (252..259).
 __device__ __forceinline__ uint32_t sr_offset(uint32_t b) { return ((b ^ 0xFFu) << 14) | 0x3FFFu; }
-// sr_offset of byte c (0..3) of a word, given the word's complement nw.
-__device__ __forceinline__ uint32_t sr_offset_nw(uint32_t nw, int c) {
-  return (((nw >> (8 * c)) & 0xFFu) << 14) | 0x3FFFu;
+// sr_offset of byte c (0..3) of the word w.
+__device__ __forceinline__ uint32_t sr_offset_w(uint32_t w, int c) {
+  return ((((w >> (8 * c)) & 0xFFu) ^ 0xFFu) << 14) | 0x3FFFu;
 }
 __device__ __forceinline__ uint32_t sr_code252(float abs_p, uint32_t offset) {
   const float w = fminf(abs_p, 6.0f);
@@ -266,6 +266,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// Bulk (non-tensor) copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing `bytes` transactions on
+// `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+               "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 // Generic-proxy writes to shared memory by this thread, ordered before later

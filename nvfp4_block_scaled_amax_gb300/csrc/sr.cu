@@ -60,14 +60,14 @@ constexpr uint32_t kCode252x8 = 252u * 0x11111111u;
 
 // Codes of row k of the sub-block (column c in nibble c) times the factor
 // of column c, fr[c] (1D column-wise: the column's factor; otherwise one
-// factor for the row), with the row's random bytes (complemented: nrb).
+// factor for the row), with the row's random bytes rb.
 template <typename T>
-__device__ __forceinline__ uint32_t sr_row_word(const Sub<T>& s, int k, const float (&f)[8], const uint2& nrb,
+__device__ __forceinline__ uint32_t sr_row_word(const Sub<T>& s, int k, const float (&f)[8], const uint2& rb,
                                                 uint32_t sgn) {
   uint32_t acc = 0;
 #pragma unroll
   for (int c = 0; c < 8; ++c)
-    acc += sr_code252(__fmul_rn(fabsf(s.v(k, c)), f[c]), sr_offset_nw(c < 4 ? nrb.x : nrb.y, c & 3)) << (4 * c);
+    acc += sr_code252(__fmul_rn(fabsf(s.v(k, c)), f[c]), sr_offset_w(c < 4 ? rb.x : rb.y, c & 3)) << (4 * c);
   return (acc - kCode252x8) | sgn;
 }
 
@@ -112,16 +112,14 @@ __device__ __forceinline__ void sr_pass(uint32_t stage, const float* rtab_row, c
   load_sub<T>(stage, bx, trow, j, s);
 
   const int64_t M = a.M, N = a.N, y0 = r0 + trow, x0 = c0 + tcol;
-  // the sub-block's random bytes, complemented (the encoder's form): row k
-  // at rb[k], column c in byte c; outside x they are the zero fill, unused
+  // the sub-block's random bytes: row k at rb[k], column c in byte c;
+  // outside x they are the zero fill, unused
   uint2 rb[8];
   const uint32_t rstage = stage + (uint32_t)tile_bytes<T>();
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int r = trow + k;
     rb[k] = lds64(rstage + (uint32_t)(r * 128 + ((((tcol >> 4) ^ (r & 7)) << 4) | (tcol & 8))));
-    rb[k].x = ~rb[k].x;
-    rb[k].y = ~rb[k].y;
   }
 
   const int64_t srow = N / 2, scol = M / 2;
