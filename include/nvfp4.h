@@ -206,6 +206,33 @@ nvfp4_status nvfp4_quantize_grouped_1d(const void* x, int dtype, int64_t N, int 
 nvfp4_status nvfp4_quantize_grouped_2d(const void* x, int dtype, int64_t N, int num_groups,
                                        const int64_t* group_rows, const nvfp4_output* outs,
                                        unsigned flags, const float* noop, void* stream);
+/*
+ * Single-launch grouped 1D / 2D quantize: the results of
+ * nvfp4_quantize_grouped_1d / _2d (every member's amax in both of its
+ * buffers, its codes and scales) from one persistent kernel that reads x
+ * from HBM once: the tiles of all members stream through shared memory while
+ * each CTA keeps a maximum per member, a grid-wide barrier combines the
+ * members' maxima in the workspace, then every member's tiles are cast with
+ * that member's global scale.  (The same pages as the grouped quantize; the
+ * single launch is nvfp4_quantize_1d_single_pass's design applied to every
+ * member at once.)
+ *   Arguments and checks as nvfp4_quantize_grouped_1d; x BF16 (FP32:
+ *   NVFP4_ERR_DTYPE); flags ROWWISE | COLWISE | SWIZZLED (no SKIP_AMAX).
+ *   workspace: as for nvfp4_quantize_1d_single_pass (4096 bytes, zeroed
+ *   before first use, not shared by calls that can run at the same time);
+ *   besides the 64-byte barrier header this call uses bytes 64..583 (two
+ *   banks of per-member maxima, each cleared by the call that used it, so
+ *   single-pass calls of either kind may share one workspace).  After a call
+ *   that reported NVFP4_ERR_TIMEOUT, zero it again.
+ */
+nvfp4_status nvfp4_quantize_grouped_1d_single_pass(const void* x, int dtype, int64_t N, int num_groups,
+                                                   const int64_t* group_rows, const nvfp4_output* outs,
+                                                   unsigned flags, const float* noop, void* workspace,
+                                                   void* stream);
+nvfp4_status nvfp4_quantize_grouped_2d_single_pass(const void* x, int dtype, int64_t N, int num_groups,
+                                                   const int64_t* group_rows, const nvfp4_output* outs,
+                                                   unsigned flags, const float* noop, void* workspace,
+                                                   void* stream);
 
 /*
  * NVFP4 quantize with the random Hadamard transform on the column-wise path
@@ -234,7 +261,8 @@ nvfp4_status nvfp4_quantize_rht(const void* x, int dtype, int64_t M, int64_t N,
  *   before its first use and not shared by calls that can run at the same
  *   time; the kernel leaves it ready for the next call (it uses the first 64
  *   bytes: the grid barrier's generation and, for two alternating
- *   generations, an arrival count and two maxima; the rest is reserved).
+ *   generations, an arrival count and two maxima; the grouped single-pass
+ *   quantize also uses bytes 64..583; the rest is reserved).
  *   After a call that reported NVFP4_ERR_TIMEOUT through
  *   nvfp4_device_status, zero it again.
  *   flags: ROWWISE | COLWISE | SWIZZLED (no SKIP_AMAX: use the two-pass

@@ -11,7 +11,7 @@ Hadamard transform, dequantize) runs in the library's CUDA kernels.
 Modes: "1d" (1x16 blocks), "2d" (16x16 tiles), "rht" (random Hadamard
 transform on the column-wise path) and "row_scaled" (one amax per row,
 row-wise only).  ``quantize_grouped`` quantizes several tensors stacked along
-the first dimension, each with its own amax, in three launches;
+the first dimension, each with its own amax (one launch for bfloat16);
 ``quantize_sr`` rounds the codes stochastically with caller-supplied random
 bytes.
 
@@ -351,13 +351,17 @@ def quantize_sr(x: torch.Tensor, rbits: torch.Tensor, mode: str = "1d", rowwise:
 
 def quantize_grouped(x: torch.Tensor, splits, mode: str = "1d", rowwise: bool = True, colwise: bool = True,
                      swizzled: bool = False, out: list[NVFP4Tensor] | None = None, skip_amax: bool = False,
-                     noop: torch.Tensor | None = None) -> list[NVFP4Tensor]:
+                     noop: torch.Tensor | None = None, path: str = "auto",
+                     workspace: torch.Tensor | None = None) -> list[NVFP4Tensor]:
     """Grouped (multi-tensor) quantize: x (M x N, bfloat16 or float32) stacks
     len(splits) member tensors along its first dimension, member g being the
     splits[g] rows after the earlier members'.  Each member is quantized as a
     tensor of its own (its own amax, its own transpose) into its own
-    NVFP4Tensor; three kernel launches whatever the number of members.
-    mode: "1d" or "2d".  out: one NVFP4Tensor per member (default: allocated)."""
+    NVFP4Tensor.  mode: "1d" or "2d".  out: one NVFP4Tensor per member
+    (default: allocated).  path: "single_pass" (one persistent kernel, x read
+    from HBM once; bfloat16, no skip_amax; the workspace as for ``quantize``),
+    "three_pass" (zero the amaxes, max|x| per member, cast) or "auto" (single
+    pass where it applies)."""
     if x.dim() != 2:
         raise ValueError("x must be 2-D (M x N)")
     if mode not in ("1d", "2d"):
@@ -378,12 +382,24 @@ def quantize_grouped(x: torch.Tensor, splits, mode: str = "1d", rowwise: bool = 
     _require_cuda(x, noop)
     flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLED if swizzled else 0) | \
         (SKIP_AMAX if skip_amax else 0)
+    if path not in ("auto", "single_pass", "three_pass"):
+        raise ValueError(f"unknown path {path!r}")
+    single = x.dtype == torch.bfloat16 and not skip_amax and path != "three_pass"
+    if path == "single_pass" and not single:
+        raise ValueError("the single-pass grouped quantize takes bfloat16 x and no skip_amax")
     rows = (ctypes.c_int64 * len(splits))(*splits)
     outs = (_lib.Output * len(out))(*[q.c_struct() for q in out])
     L = _lib.load()
-    fn = L.nvfp4_quantize_grouped_1d if mode == "1d" else L.nvfp4_quantize_grouped_2d
     with _OnDevice(x.device):
-        rc = fn(_ptr(x), _dtype_code(x), N, len(splits), rows, outs, flags, _ptr(noop), _stream(x.device))
+        s = _stream(x.device)
+        if single:
+            ws = workspace if workspace is not None else single_pass_workspace(x.device, s.value)
+            _require_cuda(ws)
+            fn = L.nvfp4_quantize_grouped_1d_single_pass if mode == "1d" else L.nvfp4_quantize_grouped_2d_single_pass
+            rc = fn(_ptr(x), _dtype_code(x), N, len(splits), rows, outs, flags, _ptr(noop), _ptr(ws), s)
+        else:
+            fn = L.nvfp4_quantize_grouped_1d if mode == "1d" else L.nvfp4_quantize_grouped_2d
+            rc = fn(_ptr(x), _dtype_code(x), N, len(splits), rows, outs, flags, _ptr(noop), s)
     _lib.check(rc, f"nvfp4 grouped quantize ({mode})")
     return out
 

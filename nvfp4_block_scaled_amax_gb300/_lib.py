@@ -22,6 +22,7 @@ EXPORTS = ("nvfp4_status_string", "nvfp4_scale_bytes", "nvfp4_compute_amax", "nv
            "nvfp4_quantize_1d", "nvfp4_quantize_2d", "nvfp4_quantize_row_scaled", "nvfp4_quantize_rht",
            "nvfp4_quantize_1d_single_pass", "nvfp4_quantize_2d_single_pass", "nvfp4_quantize_rht_single_pass",
            "nvfp4_quantize_2d_single_pass_noalloc", "nvfp4_quantize_grouped_1d", "nvfp4_quantize_grouped_2d",
+           "nvfp4_quantize_grouped_1d_single_pass", "nvfp4_quantize_grouped_2d_single_pass",
            "nvfp4_quantize_1d_sr", "nvfp4_quantize_2d_sr",
            "nvfp4_dequantize", "nvfp4_swizzle_scales", "nvfp4_device_status")
 SINGLE_PASS_WORKSPACE_BYTES = 4096
@@ -69,6 +70,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         for name in ("nvfp4_quantize_grouped_1d", "nvfp4_quantize_grouped_2d"):
             getattr(L, name).argtypes = [vp, c_int, i64, c_int, ctypes.POINTER(i64), ctypes.POINTER(Output), uint,
                                          vp, vp]
+        for name in ("nvfp4_quantize_grouped_1d_single_pass", "nvfp4_quantize_grouped_2d_single_pass"):
+            getattr(L, name).argtypes = [vp, c_int, i64, c_int, ctypes.POINTER(i64), ctypes.POINTER(Output), uint,
+                                         vp, vp, vp]
         L.nvfp4_dequantize.argtypes = [vp, vp, vp, i64, i64, uint, vp, c_int, vp]
         L.nvfp4_swizzle_scales.argtypes = [vp, vp, i64, i64, vp]
         L.nvfp4_device_status.argtypes = [ctypes.POINTER(u32), c_int]

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int n = (a.num_tiles - 1 - b) / G + 1;  // tiles t_k = b + k * G, k < n (grid <= tiles)
   const int kept_from = n > S ? n - S : 0;
   const sp::StageRing<uint16_t, S, WPT> ring{sm.stages, sm.full, sm.loaded, sm.issued, sm.tile_in, &tmap, b, G,
-                                             a.tiles_n, a.status};
+                                             sp::PlainTiles{a.tiles_n}, a.status};
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   fill_hadamard_operand(sm.hmat, 256, a.sign_mask);
   fence_proxy_async_shared();  // the operand, before the tensor cores read it
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
 template <bool kBulk>
 cudaError_t launch_rht_t(const CUtensorMap& map, const CastArgs& a, SinglePassWorkspace* ws, const LaunchCtx& ctx) {
-  return sp::launch_persistent<fused_rht_kernel<kBulk>>(rht_smem_bytes(), kRThreads, map, a, ws, ctx);
+  return sp::launch_persistent<fused_rht_kernel<kBulk>>(rht_smem_bytes(), kRThreads, map, a, a.num_tiles, ws, ctx);
 }
 
 }  // namespace

@@ -32,19 +32,6 @@ constexpr int kGThreads = 256;  // amax and cast kernels
 constexpr int kGUnroll = 8;     // 16-byte loads in flight per thread and chunk
 static_assert(kGroupChunkVecs == (int64_t)kGThreads * kGUnroll, "chunk = one batch of the CTA's loads");
 
-// Largest g with start[g] <= i (start[0] = 0 <= i < start[n]).
-__device__ __forceinline__ int member_of(const int* start, int n, int i) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (start[mid] <= i)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  return lo;
-}
-
 __global__ void grouped_zero_kernel(const __grid_constant__ GroupedArgs ga) {
   grid_launch_dependents();
   if (ga.noop != nullptr && *ga.noop == 1.0f) return;
@@ -168,21 +155,6 @@ __device__ __forceinline__ GSmem gcarve(uint8_t* raw) {
   return s;
 }
 
-// Tile t of all members: its member g and its position in that member.
-struct TilePos {
-  int g;
-  int64_t r0, c0;  // in the member
-};
-__device__ __forceinline__ TilePos tile_pos(const GroupedArgs& ga, int t) {
-  TilePos p;
-  p.g = member_of(ga.tile_start, ga.num_groups, t);
-  const int lt = t - ga.tile_start[p.g];
-  const int tr = lt / ga.tiles_n, tc = lt - tr * ga.tiles_n;
-  p.r0 = (int64_t)tr * kTile;
-  p.c0 = (int64_t)tc * kTile;
-  return p;
-}
-
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kGThreads, TileCfg<T>::kMinBlocks)
     grouped_cast_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ GroupedArgs ga) {
@@ -207,7 +179,7 @@ __global__ void __launch_bounds__(kGThreads, TileCfg<T>::kMinBlocks)
   __syncthreads();
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int k) {
-    const TilePos p = tile_pos(ga, tile_of(k));
+    const MemberTile p = member_tile(ga, tile_of(k));
     uint8_t* dst = sm.stages + (size_t)(k % C::kStages) * tile_bytes<T>();
     uint64_t* bar = &sm.bars[k % C::kStages];
     mbar_arrive_expect_tx(bar, tile_bytes<T>());
@@ -227,7 +199,7 @@ __global__ void __launch_bounds__(kGThreads, TileCfg<T>::kMinBlocks)
   int k = 0;
   for (; k < my_count; ++k) {
     const int s = k % C::kStages;
-    const TilePos p = tile_pos(ga, tile_of(k));  // the same in every thread
+    const MemberTile p = member_tile(ga, tile_of(k));  // the same in every thread
     if (p.g != cur) {
       // every thread is past the previous tile's cast (the barrier at the end
       // of its iteration), so the tables may be rewritten
@@ -315,8 +287,7 @@ cudaError_t launch_cast_t(const CUtensorMap& map, const GroupedArgs& ga, bool pd
 
 }  // namespace
 
-cudaError_t launch_grouped(const void* x, const CUtensorMap* map, bool bf16, int mode, GroupedArgs ga,
-                           bool skip_amax, const LaunchCtx& ctx) {
+void grouped_prefix_sums(GroupedArgs& ga, bool bf16) {
   const int epv = bf16 ? 8 : 4;
   ga.tiles_n = (int)((ga.N + kTile - 1) / kTile);
   ga.tile_start[0] = 0;
@@ -329,10 +300,19 @@ cudaError_t launch_grouped(const void* x, const CUtensorMap* map, bool bf16, int
   }
   ga.num_tiles = ga.tile_start[ga.num_groups];
   ga.num_chunks = ga.chunk_start[ga.num_groups];
+}
+
+cudaError_t launch_grouped_zero(const GroupedArgs& ga, const LaunchCtx& ctx) {
+  grouped_zero_kernel<<<1, kMaxGroups, 0, ctx.stream>>>(ga);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped(const void* x, const CUtensorMap* map, bool bf16, int mode, GroupedArgs ga,
+                           bool skip_amax, const LaunchCtx& ctx) {
+  grouped_prefix_sums(ga, bf16);
   cudaError_t e;
   if (!skip_amax) {
-    grouped_zero_kernel<<<1, kMaxGroups, 0, ctx.stream>>>(ga);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_grouped_zero(ga, ctx)) != cudaSuccess) return e;
     if (ga.num_chunks > 0) {
       const void* fn = bf16 ? (const void*)grouped_amax_kernel<true> : (const void*)grouped_amax_kernel<false>;
       static std::atomic<int> occ[2] = {0, 0};  // CTAs per SM

@@ -283,14 +283,17 @@ static_assert(NVFP4_MAX_GROUPS == kMaxGroups, "member table size");
 
 // Grouped quantize: every member is checked as a plain quantize of its rows
 // (its slice of x and its outputs), then the member table is filled.
+// With a workspace, the single-launch form (BF16, no SKIP_AMAX).
 nvfp4_status quantize_grouped(int mode, const void* x, int dtype, int64_t N, int num_groups,
                               const int64_t* group_rows, const nvfp4_output* outs, unsigned flags,
-                              const float* noop, void* stream) {
+                              const float* noop, void* workspace, bool single_pass, void* stream) {
   if (group_rows == nullptr || outs == nullptr) return NVFP4_ERR_NULL;
   if (num_groups < 1 || num_groups > kMaxGroups) return NVFP4_ERR_SHAPE;
   if (dtype != NVFP4_BF16 && dtype != NVFP4_FP32) return NVFP4_ERR_DTYPE;
+  if (single_pass && dtype != NVFP4_BF16) return NVFP4_ERR_DTYPE;
   if (N < 0 || N >= kMaxDim || N % 16 != 0) return NVFP4_ERR_SHAPE;
-  const unsigned allowed = NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SWIZZLED | NVFP4_SKIP_AMAX;
+  const unsigned allowed =
+      NVFP4_ROWWISE | NVFP4_COLWISE | NVFP4_SWIZZLED | (single_pass ? 0u : (unsigned)NVFP4_SKIP_AMAX);
   const bool row = flags & NVFP4_ROWWISE, col = flags & NVFP4_COLWISE;
   const int64_t eb = dtype == NVFP4_BF16 ? 2 : 4;
   GroupedArgs ga = {};
@@ -325,6 +328,8 @@ nvfp4_status quantize_grouped(int mode, const void* x, int dtype, int64_t N, int
       seen[n_seen++] = p;
     }
   if (noop != nullptr && !aligned16(noop)) return NVFP4_ERR_ALIGN;
+  if (single_pass && workspace == nullptr) return NVFP4_ERR_NULL;
+  if (single_pass && !aligned16(workspace)) return NVFP4_ERR_ALIGN;
   LaunchCtx ctx;
   nvfp4_status st = make_ctx(stream, &ctx);
   if (st != NVFP4_OK) return st;
@@ -335,9 +340,12 @@ nvfp4_status quantize_grouped(int mode, const void* x, int dtype, int64_t N, int
   ga.rowwise = row;
   ga.colwise = col;
   ga.swizzled = (flags & NVFP4_SWIZZLED) != 0;
-  CUtensorMap map;
+  CUtensorMap map = {};
   const bool any = total > 0 && N > 0;
   if (any && (st = x_map(x, dtype == NVFP4_BF16, total, N, &map)) != NVFP4_OK) return st;
+  if (single_pass)
+    return from_cuda(
+        launch_grouped_single_pass(map, mode, ga, static_cast<SinglePassWorkspace*>(workspace), ctx));
   return from_cuda(launch_grouped(x, any ? &map : nullptr, dtype == NVFP4_BF16, mode, ga,
                                   (flags & NVFP4_SKIP_AMAX) != 0, ctx));
 }
@@ -544,13 +552,27 @@ nvfp4_status nvfp4_quantize_2d_sr(const void* x, int dtype, int64_t M, int64_t N
 nvfp4_status nvfp4_quantize_grouped_1d(const void* x, int dtype, int64_t N, int num_groups,
                                        const int64_t* group_rows, const nvfp4_output* outs, unsigned flags,
                                        const float* noop, void* stream) {
-  return quantize_grouped(kCast1D, x, dtype, N, num_groups, group_rows, outs, flags, noop, stream);
+  return quantize_grouped(kCast1D, x, dtype, N, num_groups, group_rows, outs, flags, noop, nullptr, false, stream);
 }
 
 nvfp4_status nvfp4_quantize_grouped_2d(const void* x, int dtype, int64_t N, int num_groups,
                                        const int64_t* group_rows, const nvfp4_output* outs, unsigned flags,
                                        const float* noop, void* stream) {
-  return quantize_grouped(kCast2D, x, dtype, N, num_groups, group_rows, outs, flags, noop, stream);
+  return quantize_grouped(kCast2D, x, dtype, N, num_groups, group_rows, outs, flags, noop, nullptr, false, stream);
+}
+
+nvfp4_status nvfp4_quantize_grouped_1d_single_pass(const void* x, int dtype, int64_t N, int num_groups,
+                                                   const int64_t* group_rows, const nvfp4_output* outs,
+                                                   unsigned flags, const float* noop, void* workspace,
+                                                   void* stream) {
+  return quantize_grouped(kCast1D, x, dtype, N, num_groups, group_rows, outs, flags, noop, workspace, true, stream);
+}
+
+nvfp4_status nvfp4_quantize_grouped_2d_single_pass(const void* x, int dtype, int64_t N, int num_groups,
+                                                   const int64_t* group_rows, const nvfp4_output* outs,
+                                                   unsigned flags, const float* noop, void* workspace,
+                                                   void* stream) {
+  return quantize_grouped(kCast2D, x, dtype, N, num_groups, group_rows, outs, flags, noop, workspace, true, stream);
 }
 
 nvfp4_status nvfp4_dequantize(const uint8_t* data, const uint8_t* scale, const float* amax, int64_t rows,

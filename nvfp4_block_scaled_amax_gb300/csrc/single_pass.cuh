@@ -57,13 +57,24 @@ __device__ __forceinline__ bool warp_wait_slot(const int* p, int want, unsigned*
   return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
 }
 
+// TMA coordinates (x = first column, y = first row) of tile t of a plain
+// tensor with tiles_n tile columns (row-major tile order).
+struct PlainTiles {
+  int tiles_n;
+  __device__ __forceinline__ void xy(int t, int32_t& x, int32_t& y) const {
+    const int tr = t / tiles_n;
+    x = (t - tr * tiles_n) * kTile;
+    y = tr * kTile;
+  }
+};
+
 // The ring of S shared-memory stages a CTA streams its tiles through: tile k
 // of the CTA (t_k = b + k * G) uses stage k % S; its TMA completion is
 // full[s] with phase parity (k / S) & 1 (the fills of a stage are
 // sequential: in phase A fill number k / S, in phase B a stage's F phase-A
 // fills are followed by its tiles in reverse, tile s + m S as fill
 // 2F - 2 - m, the same parity).
-template <typename T, int S, int WPT>
+template <typename T, int S, int WPT, class Tiles = PlainTiles>
 struct StageRing {
   uint8_t* stages;
   uint64_t* full;     // [S]
@@ -71,14 +82,16 @@ struct StageRing {
   unsigned* issued;   // [S] loads issued into the stage so far
   int* tile_in;       // [S] tile index of the stage's latest issued load
   const CUtensorMap* tmap;
-  int b, G, tiles_n;
+  int b, G;
+  Tiles tiles;        // where tile t lies in the tensor map
   unsigned* status;
 
+  // Tile k's first row and column in the tensor map.
   __device__ __forceinline__ void tile_rc(int k, int64_t& r0, int64_t& c0) const {
-    const int t = b + k * G;
-    const int tr = t / tiles_n, tc = t - tr * tiles_n;
-    r0 = (int64_t)tr * kTile;
-    c0 = (int64_t)tc * kTile;
+    int32_t x, y;
+    tiles.xy(b + k * G, x, y);
+    r0 = y;
+    c0 = x;
   }
   __device__ __forceinline__ uint32_t stage(int s) const {
     return smem_u32(stages + (size_t)s * tile::tile_bytes<T>());
@@ -95,15 +108,15 @@ struct StageRing {
   // One thread: load tile k into its stage.
   __device__ __forceinline__ void issue(int k, uint64_t pol) const {
     const int s = k % S;
-    int64_t r0, c0;
-    tile_rc(k, r0, c0);
+    int32_t c0, r0;
+    tiles.xy(b + k * G, c0, r0);
     uint8_t* dst = stages + (size_t)s * tile::tile_bytes<T>();
     issued[s] += 1;
     *reinterpret_cast<volatile int*>(&tile_in[s]) = k;  // before the arrival (see wait_full)
     mbar_arrive_expect_tx(&full[s], tile::tile_bytes<T>());
 #pragma unroll
     for (int bb = 0; bb < TileCfg<T>::kBoxes; ++bb)
-      tma_load_2d(dst + bb * kBoxBytes, tmap, (int32_t)c0 + bb * TileCfg<T>::kBoxCols, (int32_t)r0, &full[s], pol);
+      tma_load_2d(dst + bb * kBoxBytes, tmap, c0 + bb * TileCfg<T>::kBoxCols, r0, &full[s], pol);
   }
   // Warp (all lanes): done with stage s's tile.  The group's last warp
   // loads tile `next` (if any) into the stage.  `token` is a value each lane
@@ -214,8 +227,8 @@ __device__ __forceinline__ void bulk_free(int& pending_q, unsigned* wb) {
 // cooperative launch so that all CTAs are co-resident (the grid barrier
 // needs them all).  The dynamic shared-memory limit is raised once per
 // kernel and device.
-template <auto Fn>
-cudaError_t launch_persistent(size_t smem, int threads, const CUtensorMap& map, const CastArgs& a,
+template <auto Fn, class Args>
+cudaError_t launch_persistent(size_t smem, int threads, const CUtensorMap& map, const Args& a, int num_tiles,
                               SinglePassWorkspace* ws, const LaunchCtx& ctx) {
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
@@ -227,7 +240,7 @@ cudaError_t launch_persistent(size_t smem, int threads, const CUtensorMap& map, 
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit);
   }
-  const int grid = a.num_tiles < ctx.num_sms ? a.num_tiles : ctx.num_sms;
+  const int grid = num_tiles < ctx.num_sms ? num_tiles : ctx.num_sms;
   if (grid == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -243,6 +243,23 @@ def test_grouped_validation(lib):
     assert grouped([128], o=members(1, {0: dict(amax_col=0x1000000 + 0x200000)})) == ERR_FLAGS
     assert grouped([128], noop=NOOP + 4) == ERR_ALIGN
 
+    # the single-launch form: the same checks, then BF16 only, no SKIP_AMAX,
+    # and a 16-byte aligned workspace
+    for fn in (lib.nvfp4_quantize_grouped_1d_single_pass, lib.nvfp4_quantize_grouped_2d_single_pass):
+        def sp(rows, dtype=0, flags=ROW | COL, ws=A, o=None, x=X):
+            r = (ctypes.c_int64 * len(rows))(*rows)
+            o = members(len(rows)) if o is None else o
+            return fn(x, dtype, 256, len(rows), r, o, flags, None, ws, None)
+        assert sp([128, 24]) == ERR_SHAPE
+        assert sp([128] * 65) == ERR_SHAPE
+        assert sp([128], dtype=1) == ERR_DTYPE                        # FP32: the three-launch entry points
+        assert sp([128], flags=ROW | COL | SKIP) == ERR_FLAGS           # a given amax: the three-launch form
+        assert sp([128], ws=None) == ERR_NULL
+        assert sp([128], ws=A + 4) == ERR_ALIGN
+        assert sp([128, 64], flags=ROW | COL | SWZ) == ERR_ALIGN
+        assert sp([128, 128], o=members(2, {1: dict(amax_row=0x1000000 + 0x200000)})) == ERR_FLAGS
+        assert sp([128], x=X + 8) == ERR_ALIGN
+
 
 def test_python_layer_rejects_cpu_tensors():
     import torch
