@@ -7,7 +7,8 @@ that sized all of its device memory up front.  For them the library keeps
 the single-pass kernel's scratch in a static array of its own.  This test
 calls that entry point through the C ABI twice in a row (the array keeps
 the previous call's contents) and checks each result against the regular
-single-pass entry point, which uses a caller-allocated workspace.  It lives
+single-pass entry point, which uses a caller-allocated workspace, and
+against the oracle.  It lives
 in its own file, collected last, so a run that stops at the first failure
 has already run every other test.
 """
@@ -18,6 +19,7 @@ import torch
 
 import nvfp4_block_scaled_amax_gb300 as nv
 from nvfp4_block_scaled_amax_gb300 import _lib, inputs
+from nvfp4_testutil import assert_quantize_equal, bits
 
 pytestmark = pytest.mark.gpu
 
@@ -42,17 +44,19 @@ def _same(a, b):
         assert torch.equal(ta, tb), name   # the 2D codec is exact: no tolerance
 
 
-def test_noalloc_matches_single_pass_on_consecutive_calls():
+def test_noalloc_matches_single_pass_on_consecutive_calls(oracle_mod):
     torch.cuda.set_device(0)
     M, N = 2048, 1536
-    x1 = inputs.outliers(M, N, seed=41, frac=0.01).cuda()
-    x2 = (inputs.randn(M, N, seed=42) * 0.25).to(torch.bfloat16).cuda()   # a smaller maximum
-    for x in (x1, x2):                       # two calls in a row on the shared array
+    x1 = inputs.outliers(M, N, seed=41, frac=0.01)
+    x2 = (inputs.randn(M, N, seed=42) * 0.25).to(torch.bfloat16)   # a smaller maximum
+    for step, xh in enumerate((x1, x2)):     # two calls in a row on the shared array
+        x = xh.cuda()
         got = _outputs(M, N)
         _noalloc(x, got, ROW | COL | SWZ)
         ref = nv.quantize(x, "2d", swizzled=True, path="single_pass")
         torch.cuda.synchronize()
         _same(got, ref)
+        assert_quantize_equal(oracle_mod, got, oracle_mod.quantize("2d", bits(xh)), True, what=f"no-alloc call {step}")
 
 
 def test_noalloc_rejects_bad_arguments_without_launching():
