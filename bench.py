@@ -385,30 +385,97 @@ def bench_ours(args, rank, world, local_rank):
 
 
 def bench_e2e(nv, spec, x_host, q, mask, args, dev, flush):
-    """Same metric through the public API with host buffers: pinned host x ->
-    device, quantize, all outputs -> pinned host, every step timed."""
+    """Same metric through the public API with host buffers: every step copies
+    its input from pinned host memory to the device, quantizes it and copies
+    all of its outputs back to pinned host memory, inside the timed region.
+    Measured two ways: one step at a time (copy in, quantize, copy out,
+    serialised; L2 flushed between steps; mean per step), and as a stream of
+    steps on two device buffer sets and three streams, so that step k + 1's
+    copy in overlaps step k's quantize and copy out (the host link carries
+    both directions at once); `value` is the stream's: K steps' bytes over
+    the time from the first copy in to the last copy out."""
     import torch
     stream = torch.cuda.current_stream(dev)
     xh = x_host.pin_memory()
+    colwise = spec["mode"] != "row_scaled"
+
+    def outputs(qq):
+        return [t for t in (qq.data_row, qq.scale_row, qq.amax_row, qq.data_col, qq.scale_col, qq.amax_col)
+                if t is not None]
+
+    def quantize(xd, qq):
+        nv.quantize(xd, spec["mode"], rowwise=True, colwise=colwise, swizzled=spec["swizzled"],
+                    sign_mask=mask, out=qq)
+
     xd = torch.empty_like(xh, device=dev)
-    outs = [t for t in (q.data_row, q.scale_row, q.amax_row, q.data_col, q.scale_col, q.amax_col) if t is not None]
+    outs = outputs(q)
     hosts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = xh.numel() * xh.element_size()
     d2h = sum(t.numel() * t.element_size() for t in outs)
 
     def step():
         xd.copy_(xh, non_blocking=True)
-        nv.quantize(xd, spec["mode"], rowwise=True, colwise=spec["mode"] != "row_scaled",
-                    swizzled=spec["swizzled"], sign_mask=mask, out=q)
+        quantize(xd, q)
         for h, t in zip(hosts, outs):
             h.copy_(t, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         step()
     times = time_steps(step, args.steps, flush, stream)
-    ms = statistics.mean(times)
-    return {"value": round(workload_bytes(spec) / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+    ms_serial = statistics.mean(times)
+
+    # the stream of steps: buffer set k % 2; events order each set's reuse
+    sets = []
+    for _ in range(2):
+        qq = nv.empty(spec["M"], spec["N"], colwise=colwise, row_scaled=spec["mode"] == "row_scaled",
+                      swizzled=spec["swizzled"], device=dev)
+        oo = outputs(qq)
+        sets.append({"x": torch.empty_like(xh, device=dev), "q": qq, "outs": oo,
+                     "hosts": [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in oo],
+                     "in": torch.cuda.Event(), "done": torch.cuda.Event(), "out": torch.cuda.Event()})
+    s_in, s_q, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    for st in sets:  # every event recorded once, so that the first waits are satisfied
+        for ev in ("in", "done", "out"):
+            st[ev].record(stream)
+
+    def enqueue(k):
+        st = sets[k % 2]
+        s_in.wait_event(st["done"])       # step k - 2's quantize has read this input buffer
+        with torch.cuda.stream(s_in):
+            st["x"].copy_(xh, non_blocking=True)
+            st["in"].record(s_in)
+        s_q.wait_event(st["in"])
+        s_q.wait_event(st["out"])         # step k - 2's outputs have been copied out
+        with torch.cuda.stream(s_q):
+            quantize(st["x"], st["q"])
+            st["done"].record(s_q)
+        s_out.wait_event(st["done"])
+        with torch.cuda.stream(s_out):
+            for h, t in zip(st["hosts"], st["outs"]):
+                h.copy_(t, non_blocking=True)
+            st["out"].record(s_out)
+
+    n = max(args.steps, 6)
+    for k in range(4):
+        enqueue(k)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for k in range(n):
+        enqueue(k)
+    for st_ in (s_in, s_q):
+        s_out.wait_stream(st_)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    ms_stream = t0.elapsed_time(t1) / n
+    wb = workload_bytes(spec)
+    return {"value": round(wb / (ms_stream / 1e3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_stream, 4),
+            "how": f"{n} steps streamed on two buffer sets: step k+1's copy in overlaps step k's quantize "
+                   "and copy out (three CUDA streams, pinned host buffers)",
+            "serial": {"value": round(wb / (ms_serial / 1e3) / 1e9, 1), "unit": "GB/s",
+                       "ms_per_step": round(ms_serial, 4),
+                       "how": "one step at a time: copy in, quantize, copy out; L2 flushed between steps"}}
 
 
 def bench_variants(nv, inputs, args, dev, flush, stream):
