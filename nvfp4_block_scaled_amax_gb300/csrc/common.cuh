@@ -128,6 +128,12 @@ __device__ __forceinline__ uint32_t e2m1_sr(float p, uint32_t offset) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// max(|a|, |b|) per BF16 half, as a packed pair (inputs are finite).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+  return r;
+}
 __device__ __forceinline__ float bf16x2_hmax_to_f32(uint32_t w) {
   return fmaxf(bf16_lo(w), bf16_hi(w));
 }
@@ -139,10 +145,24 @@ __device__ __forceinline__ float round_bf16(float v) {
   return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
 
-// In-place 16-point Walsh-Hadamard butterflies on two columns at once, each
-// value an FP32x2 pair, natural (Sylvester) order: after the four stages
-// v[o] = sum_i (-1)^popcount(o & i) v_in[i] per half (the packed adds and
-// subtracts round each half as the scalar ones would).
+// In-place 16-point Walsh-Hadamard butterflies, natural (Sylvester) order:
+// after the four stages v[o] = sum_i (-1)^popcount(o & i) v_in[i].
+__device__ __forceinline__ void fwht16(float* v) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        float a = v[i], c = v[i + h];
+        v[i] = __fadd_rn(a, c);
+        v[i + h] = __fsub_rn(a, c);
+      }
+    }
+  }
+}
+
+// The same transform on two columns at once, each value an FP32x2 pair
+// (packed adds and subtracts round each half exactly as the scalar ones).
 __device__ __forceinline__ void fwht16_x2(uint64_t* v) {
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1) {
@@ -379,6 +399,9 @@ __device__ __forceinline__ void st_cs_v2_if(void* p, uint32_t a, uint32_t b, boo
                "r"(a), "r"(b), "r"((uint32_t)pred)
                : "memory");
 }
+__device__ __forceinline__ void st_cs_u16(void* p, uint32_t a) {
+  asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(a)) : "memory");
+}
 __device__ __forceinline__ void st_cs_u8(void* p, uint32_t a) {
   asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(a & 0xFFu)) : "memory");
 }
@@ -387,6 +410,23 @@ __device__ __forceinline__ void st_cs_u8(void* p, uint32_t a) {
 // scale matrix with C columns.
 __device__ __forceinline__ int64_t swizzled_scale_offset(int64_t r, int64_t c, int64_t C) {
   return ((r >> 7) * (C >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+// Writes n (1, 2 or 4) consecutive scale bytes (packed little-endian in v)
+// of row r starting at scale column c, compact [R][C] or swizzled.  In the
+// swizzled layout c is a multiple of n, so the group is contiguous and
+// aligned; in the compact layout the store is split into bytes when the
+// address is not aligned.
+__device__ __forceinline__ void store_scales(uint8_t* base, int64_t r, int64_t c, int64_t C, bool swizzled,
+                                             int n, uint32_t v) {
+  int64_t off = swizzled ? swizzled_scale_offset(r, c, C) : r * C + c;
+  uint8_t* p = base + off;
+  if (((reinterpret_cast<uintptr_t>(p)) & (uintptr_t)(n - 1)) == 0) {
+    if (n == 4) { st_cs_u32(p, v); return; }
+    if (n == 2) { st_cs_u16(p, v); return; }
+    if (n == 1) { st_cs_u8(p, v); return; }
+  }
+  for (int i = 0; i < n; ++i) st_cs_u8(p + i, v >> (8 * i));
 }
 
 }  // namespace nvfp4

@@ -67,6 +67,12 @@ __host__ __device__ constexpr size_t smem_bytes() {
          8 * TileCfg<T>::kStages + 16;
 }
 
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in box `box` of a
+// stage: the TMA 128-byte swizzle XORs the chunk index with row % 8.
+__device__ __forceinline__ uint32_t swz(int box, int row, int chunk) {
+  return (uint32_t)(box * kBoxBytes + row * 128 + (((chunk ^ row) & 7) << 4));
+}
+
 // E4M3 scale code of a block with maximum b under global scale g.
 __device__ __forceinline__ uint32_t block_scale(float b, float g) {
   return e4m3_rn_satfinite(__fmul_rn(div6_rn(b), g));
