@@ -15,7 +15,8 @@ from nvfp4_testutil import scales_compact as _compact
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(16, 16), (128, 128), (48, 80), (208, 336), (256, 384), (384, 640), (1088, 1024)]
+SHAPES = [(16, 16), (128, 128), (48, 80), (208, 336), (256, 384), (384, 640), (1088, 1024),
+          (16, 4096), (4096, 16), (144, 2064)]  # one row block / one column block / thin ragged
 DTYPES = [torch.bfloat16, torch.float32]
 
 
@@ -69,7 +70,8 @@ def test_single_pass_workspace_reuse(oracle_mod, mode):
     assert nv.device_status() == 0
 
 
-@pytest.mark.parametrize("M,N", [(16, 16), (128, 128), (48, 80), (208, 336), (384, 640), (1088, 1024)])
+@pytest.mark.parametrize("M,N", [(16, 16), (128, 128), (48, 80), (208, 336), (384, 640), (1088, 1024),
+                                 (16, 2048), (2048, 16)])
 @pytest.mark.parametrize("path", ["two_pass", "single_pass"])
 def test_rht_matches_oracle(oracle_mod, M, N, path):
     x = _x(M, N, torch.bfloat16, seed=M + 3 * N, kind="outliers")

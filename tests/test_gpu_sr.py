@@ -14,7 +14,7 @@ from nvfp4_testutil import assert_quantize_equal, bits, np_
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(16, 16), (128, 128), (48, 80), (208, 336), (256, 384), (1088, 1024)]
+SHAPES = [(16, 16), (128, 128), (48, 80), (208, 336), (256, 384), (1088, 1024), (16, 4096), (4096, 16)]
 FLAGS = [(True, True), (True, False), (False, True)]
 
 
